@@ -1,0 +1,96 @@
+"""Pure-Python brute force of SBF insert/query, for tiny inputs only.
+
+TEST INFRASTRUCTURE ONLY.  Written independently of ``sbf_oracle.c`` (Python
+strings and integers, no shared code) so that the two can pin each other.
+
+Source: "cuSBF: A Minimizer-Aware Bloom Filter for Genomic Sequence Data on
+Modern GPUs", Sec. II-B1 (minimizer = the m-mer of minimum hash among the
+k-m+1 windows of a k-mer), Sec. II-B2 (Findere: all k-s+1 s-mers), Sec. IV-B
+(four 64-bit words per 256-bit shard, hash i in word i mod 4), Sec. IV-G
+(bit-slicing; role-specialised hashes) and Algorithms 1 and 2.  The concrete
+hash functions are this library's reading of Sec. IV-G:
+hm(x) = t ^ (t >> 32), t = (x ^ seed) * C1;  hs(x): t = (x ^ ~seed) * C1,
+t ^= t >> 32, t *= C2, t ^= t >> 29, all modulo 2^64.
+"""
+from __future__ import annotations
+
+MASK64 = (1 << 64) - 1
+C1 = 0x9E3779B97F4A7C15
+C2 = 0x6A09E667F3BCC909
+_DIGIT = {"A": "0", "C": "1", "G": "2", "T": "3"}
+
+
+def kmer_value(text: str) -> int:
+    """Base-4 number whose first digit is the first base (A0 C1 G2 T3)."""
+    return int("".join(_DIGIT[ch] for ch in text.upper()), 4)
+
+
+def is_valid(text: str) -> bool:
+    return all(ch in "ACGTacgt" for ch in text)
+
+
+def hm(x: int, seed: int) -> int:
+    t = ((x ^ seed) * C1) & MASK64
+    return t ^ (t >> 32)
+
+
+def hs(x: int, seed: int) -> int:
+    t = ((x ^ (~seed & MASK64)) * C1) & MASK64
+    t ^= t >> 32
+    t = (t * C2) & MASK64
+    t ^= t >> 29
+    return t
+
+
+def smer_words(h: int, H: int):
+    words = [0, 0, 0, 0]
+    width = 64 // H
+    for i in range(H):
+        words[i % 4] |= 1 << ((h >> (i * width)) & 63)
+    return words
+
+
+def kmer(text: str, k: int, m: int, s: int, H: int, num_shards: int, seed: int):
+    """(shard, words) of one valid k-mer given as a string of length k."""
+    minimizer = min(hm(kmer_value(text[i:i + m]), seed) for i in range(k - m + 1))
+    shard = minimizer % num_shards
+    words = [0, 0, 0, 0]
+    for j in range(k - s + 1):
+        for w, bits in enumerate(smer_words(hs(kmer_value(text[j:j + s]), seed), H)):
+            words[w] |= bits
+    return shard, words
+
+
+def records_of(seq: bytes, offsets):
+    return [(int(offsets[r]), seq[int(offsets[r]):int(offsets[r + 1])].decode("latin-1"))
+            for r in range(len(offsets) - 1)]
+
+
+def insert(seq: bytes, offsets, k, m, s, H, num_shards, seed, filt=None):
+    """Return {shard: [w0, w1, w2, w3]} with every valid k-mer inserted."""
+    filt = {} if filt is None else filt
+    for _, rec in records_of(seq, offsets):
+        for p in range(len(rec) - k + 1):
+            text = rec[p:p + k]
+            if not is_valid(text):
+                continue
+            shard, words = kmer(text, k, m, s, H, num_shards, seed)
+            cur = filt.setdefault(shard, [0, 0, 0, 0])
+            for w in range(4):
+                cur[w] |= words[w]
+    return filt
+
+
+def query(filt, seq: bytes, offsets, k, m, s, H, num_shards, seed):
+    """Return the set of absolute positions whose k-mer answers present."""
+    hits = set()
+    for start, rec in records_of(seq, offsets):
+        for p in range(len(rec) - k + 1):
+            text = rec[p:p + k]
+            if not is_valid(text):
+                continue
+            shard, words = kmer(text, k, m, s, H, num_shards, seed)
+            have = filt.get(shard, [0, 0, 0, 0])
+            if all((words[w] & ~have[w]) == 0 for w in range(4)):
+                hits.add(start + p)
+    return hits
