@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark: SBF insert + query throughput on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch: insert every k-mer of the
+workload's reference records, then query every k-mer of its reads, with the
+paper's operating point k=31, m=16, s=28, H=4.  The default workload is the
+out-of-cache configuration (1 Gbp in 10,000 contigs into a 2^36-bit = 8 GiB
+filter; 6,666,666 reads of 150 bp), the stand-in for the paper's T2T-CHM13
+experiment on which its headline throughput is quoted.
+
+Printed: one JSON line with the device-resident throughput (CUDA events on the
+launching stream, inputs already in HBM and larger than L2), the same metric
+end to end through the host-facing C-ABI calls (pinned host buffers, copies
+inside the timed region), the false-positive rate of the uniform reads, the
+roofline of the dominant kernel, SM clocks sampled during the timed region and
+the CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle arm
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from minimizer_sharded_bloom_gb300 import synth  # noqa: E402
+
+METRIC = "k-mers/s insert & query (k=31,s=28,m=16,H=4); FPR; % HBM roofline"
+K, M, S, H = 31, 16, 28, 4
+SEED = 5
+
+WORKLOADS = {
+    "out-of-cache": dict(bits=1 << 36, make=lambda: synth.out_of_cache(),
+                         desc="out-of-cache: 1 Gbp in 10,000 log-normal contigs (median 50 kbp) "
+                              "into a 2^36-bit (8 GiB) filter; query 6,666,666 x 150 bp reads "
+                              "(50% from the contigs at 1% error, 50% uniform)"),
+    "genome-like": dict(bits=1 << 30, make=lambda: synth.genome_like(),
+                        desc="genome-like: 50 Mbp with 20% copied 1-10 kbp segments at 1% error "
+                             "into a 2^30-bit (128 MiB) filter; query 1,000,000 x 150 bp reads"),
+    "irregular": dict(bits=1 << 32, make=lambda: synth.irregular(),
+                      desc="irregular: 200,000 log-normal long reads (median 8 kbp, 0.1% N in "
+                           "runs of 1-50) into a 2^32-bit filter; query a disjoint equal set"),
+    "tiny": dict(bits=1 << 20, make=lambda: synth.tiny(),
+                 desc="tiny: 100 kbp into 2^20 bits; query it plus 100 kbp uniform"),
+}
+
+# Algorithmic 32-bit integer operations per k-mer of the rolling formulation
+# (k=31, m=16, s=28, H=4), counted in the design notes: shared front end 50
+# (decode 1, validity 1, m-mer roll 1, s-mer roll 2, minimizer hash 5,
+# 3 sliding-window 64-bit minimums 12, shard 1, s-mer hash 15, four bit
+# positions to one-hot word halves 12); insert adds 10 (run compare, select,
+# OR of the new s-mer into the run's eight half-words); query adds 26 (k-mer
+# mask from four s-mer masks 16, subset test 9, answer bit 1).
+ALU_OPS_PER_KMER = {"insert": 60, "query": 76}
+# Integer peak: 152 SMs x 128 INT32 lanes x 2.07 GHz maximum SM clock.
+ALU_PEAK_TOPS = 152 * 128 * 2.07e9 / 1e12
+
+# ncu DRAM bytes (read + write) per k-mer of the out-of-cache launches, valid
+# only for the kernel source they were measured on.
+MEASURED_TRAFFIC = {"source_sha": None, "insert": None, "query": None}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("sbf_strip.cuh", "sbf_device.cuh"):
+        with open(os.path.join(ROOT, "minimizer_sharded_bloom_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kmer_count(wl, k=K):
+    return wl.kmer_positions(k)
+
+
+def runs_estimate(wl, k=K, m=M):
+    """Expected runs: density 2/(w+1) per k-mer (Sec. II-B1) plus one run
+    start per record."""
+    w = k - m + 1
+    return kmer_count(wl, k) * 2.0 / (w + 1) + wl.n_records
+
+
+def fpr_of(words: np.ndarray, qry) -> float | None:
+    rnd = qry.meta.get("is_random")
+    if rnd is None or not rnd.any():
+        return None
+    starts = qry.offsets[:-1][rnd]
+    lens = np.diff(qry.offsets)[rnd]
+    hits = total = 0
+    for c in range(0, starts.size, 1 << 16):
+        st, ln = starts[c:c + (1 << 16)], lens[c:c + (1 << 16)]
+        nk = np.maximum(ln - K + 1, 0)
+        if nk.sum() == 0:
+            continue
+        pos = np.repeat(st, nk) + (np.arange(nk.sum()) - np.repeat(np.cumsum(nk) - nk, nk))
+        bits = (words[pos >> 5] >> (pos & 31).astype(np.uint32)) & 1
+        hits += int(bits.sum())
+        total += int(pos.size)
+    return hits / total if total else None
+
+
+def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int = 300_000):
+    """The CPU oracle, as it stands, on a bounded prefix sample of the same
+    workload, all host cores."""
+    import oracle
+    cores = os.cpu_count() or 1
+    r = int(np.searchsorted(ins.offsets, ins.offsets[0] + budget_bases, side="right")) - 1
+    r = max(1, min(r, ins.n_records))
+    s_ins = synth.Workload(ins.seq[:ins.offsets[r]], ins.offsets[:r + 1])
+    rq = max(1, min(reads, qry.n_records))
+    s_q = synth.Workload(qry.seq[:qry.offsets[rq]], qry.offsets[:rq + 1])
+    F = oracle.new_filter(bits)
+    t0 = time.perf_counter()
+    oracle.insert(F, s_ins.seq, s_ins.offsets, K, M, S, H, SEED, nthreads=cores)
+    t1 = time.perf_counter()
+    oracle.query(F, s_q.seq, s_q.offsets, K, M, S, H, SEED, nthreads=cores)
+    t2 = time.perf_counter()
+    nk = kmer_count(s_ins) + kmer_count(s_q)
+    return {"value": nk / (t2 - t0), "unit": "k-mers/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {s_ins.n_bases:,} bp ({r} records) inserted, first {rq:,} reads "
+                      f"queried; {nk:,} k-mers in {t2 - t0:.1f} s",
+            "insert_kmers_per_s": kmer_count(s_ins) / (t1 - t0),
+            "query_kmers_per_s": kmer_count(s_q) / (t2 - t1)}
+
+
+def run_reference(args, workload):
+    """The reference arm: the CPU oracle on the host cores, one bounded sample
+    of the workload per step."""
+    spec = WORKLOADS[workload]
+    ins, qry = spec["make"]()
+    for _ in range(args.warmup):
+        cpu_baseline(ins, qry, spec["bits"], budget_bases=2_000_000, reads=20_000)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cb = cpu_baseline(ins, qry, spec["bits"], budget_bases=10_000_000, reads=100_000)
+        secs.append(time.perf_counter() - t0)
+        vals.append(cb["value"])
+    value = float(np.mean(vals))
+    cb["value"] = value
+    line = {"metric": METRIC, "value": value, "unit": "k-mers/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": spec["desc"], "k": K, "m": M, "s": S, "H": H,
+                       "filter_bits": spec["bits"], "timing": "host wall clock per sample"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "k-mers/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="out-of-cache", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_info()
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, args.workload)
+        return
+
+    import torch
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter, build_lib, _native as N
+
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    build_lib.build()
+    spec = WORKLOADS[args.workload]
+    ins, qry = spec["make"]()
+    nk_ins, nk_q = kmer_count(ins), kmer_count(qry)
+
+    dseq = torch.from_numpy(ins.seq).cuda()
+    doff = torch.from_numpy(ins.offsets).cuda()
+    dq = torch.from_numpy(qry.seq).cuda()
+    dqo = torch.from_numpy(qry.offsets).cuda()
+    out = torch.zeros((qry.n_bases + 31) // 32 + 1, dtype=torch.int32, device="cuda")
+    sbf = SuperBloomFilter(spec["bits"], k=K, m=M, s=S, H=H, seed=SEED)
+    if not sbf.specialized:
+        raise RuntimeError("the benchmark configuration must run its specialised kernel")
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    n_ins, n_q = ins.n_records, qry.n_records
+
+    def step():
+        N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
+        N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), n_q, out.data_ptr(), sh)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if sbf.status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
+        ev[i][1].record(stream)
+        N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), n_q, out.data_ptr(), sh)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop() if sampler else None
+    t_ins = [ev[i][0].elapsed_time(ev[i][1]) / 1e3 for i in range(args.steps)]
+    t_q = [ev[i][1].elapsed_time(ev[i][2]) / 1e3 for i in range(args.steps)]
+    total = sum(t_ins) + sum(t_q)
+    if pg:
+        t = torch.tensor([total, sum(t_ins), sum(t_q)], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total, s_ins, s_q = (float(x) for x in t)
+    else:
+        s_ins, s_q = sum(t_ins), sum(t_q)
+    if sbf.status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    words = out.cpu().numpy().view(np.uint32)
+    fpr = fpr_of(words, qry)
+    value = world * args.steps * (nk_ins + nk_q) / total
+
+    # roofline of the dominant kernel (the longer of insert and query)
+    peaks, peak_src = measured_peaks()
+    avg_ins, avg_q = s_ins / args.steps, s_q / args.steps
+    dom = "insert" if avg_ins >= avg_q else "query"
+    dom_t = max(avg_ins, avg_q)
+    dom_k = nk_ins if dom == "insert" else nk_q
+    alu_ach = ALU_OPS_PER_KMER[dom] * dom_k / dom_t / 1e12
+    sha = kernel_source_sha()
+    traffic = None
+    if MEASURED_TRAFFIC["source_sha"] == sha and MEASURED_TRAFFIC[dom] is not None \
+            and args.workload == "out-of-cache":
+        traffic = MEASURED_TRAFFIC[dom] * dom_k
+    roofline = {"bound": "alu", "kernel": f"strip_kernel<31,16,28,4,{dom}>",
+                "achieved": alu_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (int32)",
+                "frac": alu_ach / ALU_PEAK_TOPS, "traffic": traffic,
+                "peak_source": "152 SMs x 128 INT32 lanes x 2.07 GHz (recipe unit counts)",
+                "ops_per_kmer": ALU_OPS_PER_KMER[dom], "avg_launch_ms": 1e3 * dom_t}
+    runs_i, runs_q = runs_estimate(ins), runs_estimate(qry)
+    bytes_ins = ins.n_bases + 8 * (n_ins + 1) + 64 * runs_i
+    bytes_q = qry.n_bases + 8 * (n_q + 1) + 32 * runs_q + 4 * ((qry.n_bases + 31) // 32)
+    hbm = {}
+    for name, b, t in (("insert", bytes_ins, avg_ins), ("query", bytes_q, avg_q)):
+        ach = b / t / 1e9
+        hbm[name] = {"achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                     "algorithmic_bytes_per_kmer": b / (nk_ins if name == "insert" else nk_q),
+                     "peak_source": f"{peak_src} hbm_gbs"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, N, sbf, ins, qry, nk_ins + nk_q, pg, world, min(args.steps, 3))
+
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(ins, qry, spec["bits"])
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "k-mers/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64 (integer)",
+            "data": "synthetic",
+            "config": {"workload": spec["desc"], "k": K, "m": M, "s": S, "H": H, "seed": SEED,
+                       "filter_bits": spec["bits"], "insert_kmers": nk_ins, "query_kmers": nk_q,
+                       "insert_records": n_ins, "query_records": n_q,
+                       "l2": "inputs larger than L2 (sequences 1 GB each, filter 8 GiB)"
+                             if args.workload == "out-of-cache" else "see workload",
+                       "filter_between_steps": "not cleared (insert is idempotent; same work)",
+                       "replicas": world},
+            "insert_kmers_per_s": world * args.steps * nk_ins / s_ins,
+            "query_kmers_per_s": world * args.steps * nk_q / s_q,
+            "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
+            "roofline": roofline, "roofline_hbm": hbm,
+            "gpu_launches": 4 * args.steps,
+            "gpu_launches_note": "per step: offsets check + strip kernel for insert and for query",
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cb,
+            "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    sbf.close()
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
+    """Same metric through the host-facing C-ABI calls: pinned host inputs,
+    host-to-device copies and the answer's device-to-host copy inside the
+    timed region (each call synchronizes)."""
+    h_seq = torch.from_numpy(ins.seq).pin_memory()
+    h_off = torch.from_numpy(ins.offsets).pin_memory()
+    h_q = torch.from_numpy(qry.seq).pin_memory()
+    h_qo = torch.from_numpy(qry.offsets).pin_memory()
+    h_out = torch.zeros((qry.n_bases + 31) // 32 + 1, dtype=torch.int32).pin_memory()
+
+    def one():
+        N.sbf_insert_host(sbf.handle, h_seq.data_ptr(), h_off.data_ptr(), ins.n_records, 0)
+        N.sbf_query_host(sbf.handle, h_q.data_ptr(), h_qo.data_ptr(), qry.n_records,
+                         h_out.data_ptr(), 0)
+
+    one()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if pg:
+        t = torch.tensor([dt], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        dt = float(t[0])
+    h2d = ins.seq.nbytes + ins.offsets.nbytes + qry.seq.nbytes + qry.offsets.nbytes
+    d2h = 4 * ((qry.n_bases + 31) // 32)
+    return {"value": world * steps * nk_total / dt, "unit": "k-mers/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": 1e3 * dt / steps,
+            "path": "sbf_insert_host + sbf_query_host, pinned host buffers, host wall clock"}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * sbf.h -- C ABI of libsbf, a GB300 (sm_103a) Super Bloom filter for raw DNA.
+ *
+ * The method is the one of "cuSBF: A Minimizer-Aware Bloom Filter for Genomic
+ * Sequence Data on Modern GPUs" (Dortmann, Vieth, Schmidt):
+ *   - Sec. II-B1: each k-mer's minimizer -- the m-mer of minimum hash among
+ *     its w = k-m+1 windows -- selects one 256-bit shard;
+ *   - Sec. II-B2, Eq. 2 (Findere): inside that shard all k-s+1 overlapping
+ *     s-mers of the k-mer set (insert) or test (query) H bits each;
+ *   - Sec. IV-B: the filter is 2^P shards of four 64-bit words, hash index i
+ *     addresses word i mod 4;
+ *   - Sec. IV-G: bit i of an s-mer is slice i of its 64-bit hash.
+ *
+ * Fixed readings of points the paper leaves open (the CPU oracle and the CUDA
+ * kernels follow the same ones):
+ *   - bases: A/a=0, C/c=1, G/g=2, T/t=3; any other byte is invalid and a k-mer
+ *     containing one is skipped on insert and answers 0 on query (Sec. IV-F);
+ *   - a t-mer packs with its first base most significant;
+ *   - C1 = 0x9E3779B97F4A7C15 (floor(2^64/phi)), C2 = 0x6A09E667F3BCC909
+ *     (floor((sqrt2-1)*2^64) | 1); minimizer hash t = (x ^ seed) * C1,
+ *     hm = t ^ (t >> 32); s-mer hash t = (x ^ ~seed) * C1, t ^= t >> 32,
+ *     t *= C2, t ^= t >> 29 (all mod 2^64); shard = min hm & (num_shards-1);
+ *   - hash i of an s-mer sets bit ((hs >> (i * floor(64/H))) & 63) of word
+ *     i mod 4;
+ *   - records are CSR slices of one buffer; a k-mer never spans two records;
+ *   - forward strand only.
+ *
+ * Threading and streams.  Device-facing calls (sbf_insert, sbf_query,
+ * sbf_copy_bits, sbf_load_bits, sbf_clear) only enqueue work on the given
+ * stream (a cudaStream_t passed as void*; NULL = the legacy default stream)
+ * and return without synchronizing, as the paper's device-facing entry points
+ * do (Sec. IV-A).  Host-facing calls (sbf_insert_host, sbf_query_host)
+ * return after their work is complete.  A filter may be used from one host
+ * thread at a time; calls that modify a filter must be ordered by the caller
+ * with respect to every other call on it.  The filter lives on the device that
+ * was current at sbf_create; callers must make that device current.
+ *
+ * Errors.  Functions returning int return SBF_OK (0) or a negative
+ * sbf_status; sbf_create returns NULL on error.  The message of the calling
+ * thread's last error is available from sbf_last_error().  Argument errors are
+ * found on the host before anything is enqueued.  Malformed offsets (not
+ * nondecreasing, or offsets[0] < 0) can only be seen on the device: a check
+ * kernel then sets the filter's sticky status, the insert/query kernels of
+ * that call and of every later call skip all work (query output is then left
+ * unwritten), and sbf_get_status() reports SBF_ERR_BAD_OFFSETS and clears it.
+ * No kernel traps or asserts, and there is no CPU fallback: without a usable
+ * CUDA device every compute call fails with SBF_ERR_CUDA.
+ */
+#ifndef SBF_H
+#define SBF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sbf_filter sbf_filter; /* opaque; owns the device bit array */
+
+typedef enum {
+    SBF_OK = 0,
+    SBF_ERR_INVALID_ARG = -1, /* a NULL pointer, an out-of-range parameter or size */
+    SBF_ERR_CUDA = -2,        /* a CUDA runtime call or kernel launch failed */
+    SBF_ERR_OOM = -3,         /* device memory for the filter could not be allocated */
+    SBF_ERR_BAD_OFFSETS = -4  /* reported by sbf_get_status: malformed CSR offsets */
+} sbf_status;
+
+/* Create an all-zero filter of at least num_bits bits on the current device.
+ * Shard count = ceil(num_bits / 256) rounded up to a power of two (Sec. IV-B);
+ * the device array holds num_shards * 32 bytes.
+ * Requires num_bits >= 1, num_shards <= 2^40, 1 <= m <= k <= 32,
+ * 1 <= s <= k and 1 <= H <= 10 (bit-slicing needs floor(64/H) >= 6, Sec. IV-G).
+ * seed selects the hash functions (minimizer seed = seed, s-mer seed = ~seed).
+ * Returns NULL on error (SBF_ERR_INVALID_ARG / _OOM / _CUDA in sbf_last_error). */
+sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed);
+
+/* Free the device memory of f after the device finished all work (this call
+ * synchronizes the device).  NULL-safe. */
+void sbf_destroy(sbf_filter *f);
+
+/* Insert (Algorithm 1; Sec. IV-D).  seq: device pointer to bytes; offsets:
+ * device pointer to n+1 int64, nondecreasing; record r is
+ * seq[offsets[r] .. offsets[r+1]), so seq must be readable on
+ * [offsets[0], offsets[n]).  Every valid k-mer of every record is ORed into
+ * the filter; the result does not depend on record order or on how records
+ * are split across calls.  n == 0 is a no-op.  Caller keeps ownership of
+ * seq/offsets and must keep them alive until the stream reaches this work.
+ * Asynchronous on `stream`. */
+int sbf_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream);
+
+/* Query (Algorithm 2; Sec. IV-E).  Same seq/offsets contract as sbf_insert.
+ * out_bits: device pointer to uint32 words, at least ceil(offsets[n] / 32) of
+ * them (absolute indexing).  Bit g (word g >> 5, bit g & 31, LSB first) answers
+ * the k-mer that starts at absolute position g: 1 iff it is valid (inside one
+ * record, all k bases valid) and every bit of all its k-s+1 s-mers is set in
+ * its shard.  Every word in [offsets[0] >> 5, (offsets[n] + 31) >> 5) is
+ * written (positions without a valid k-mer get 0); other words are untouched.
+ * Asynchronous on `stream`. */
+int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+              uint32_t *out_bits, void *stream);
+
+/* Host-facing insert: seq and offsets are HOST pointers (pageable or
+ * pinned), same layout as sbf_insert.  The records are staged to the device in
+ * chunks through pinned buffers on two alternating streams, overlapping copies
+ * with kernels (Sec. IV-G, host FASTX staging).  Returns when the filter holds
+ * every k-mer.  `stream` (may be NULL) is made to wait for the work. */
+int sbf_insert_host(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                    void *stream);
+
+/* Host-facing query: seq/offsets/out_bits are HOST pointers, same layout and
+ * output contract as sbf_query.  Returns when out_bits is complete. */
+int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                   uint32_t *out_bits, void *stream);
+
+/* Chunk size of the host-facing calls, in sequence positions (default 2^27;
+ * rounded down to a multiple of 32; at least 32).  Smaller chunks overlap
+ * copies and kernels at a finer grain and need smaller staging buffers. */
+int sbf_set_host_chunk(sbf_filter *f, int64_t positions);
+
+/* Copy the raw image (num_shards * 32 bytes: shard-major, four little-endian
+ * uint64 words per shard, bit b of word j = (word >> b) & 1) to dst, host or
+ * device memory (cudaMemcpyDefault).  dst_bytes must be >= the image size.
+ * Asynchronous on `stream` (for pageable host dst the copy is synchronous). */
+int sbf_copy_bits(const sbf_filter *f, void *dst, uint64_t dst_bytes, void *stream);
+
+/* Replace the image with src (same layout and size as sbf_copy_bits; host or
+ * device memory).  Saves a filter together with sbf_copy_bits.  Async. */
+int sbf_load_bits(sbf_filter *f, const void *src, uint64_t src_bytes, void *stream);
+
+/* Zero the image (an empty filter).  Asynchronous on `stream`. */
+int sbf_clear(sbf_filter *f, void *stream);
+
+/* Number of 256-bit shards (a power of two); 0 for NULL. */
+uint64_t sbf_num_shards(const sbf_filter *f);
+
+/* The filter's parameters; any output pointer may be NULL. */
+int sbf_get_params(const sbf_filter *f, int *k, int *m, int *s, int *H, uint64_t *seed);
+
+/* 1 if insert/query of f run a kernel specialised at compile time for its
+ * (k, m, s, H), 0 if they run the runtime-parameter kernel (same results). */
+int sbf_is_specialized(const sbf_filter *f);
+
+/* Synchronize `stream`, then return and clear the sticky device status:
+ * SBF_OK, SBF_ERR_BAD_OFFSETS, or SBF_ERR_CUDA if the stream reported an
+ * error. */
+int sbf_get_status(sbf_filter *f, void *stream);
+
+/* Message of the calling thread's last error ("" if none). */
+const char *sbf_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SBF_H */

@@ -1,0 +1,149 @@
+"""ctypes binding of libsbf (include/sbf.h), same names, argument marshalling only.
+
+Every computation runs in the library's CUDA kernels.  If libsbf.so has not
+been built, or cannot be loaded, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build_lib
+
+SBF_OK = 0
+SBF_ERR_INVALID_ARG = -1
+SBF_ERR_CUDA = -2
+SBF_ERR_OOM = -3
+SBF_ERR_BAD_OFFSETS = -4
+
+# every entry point the header declares: name -> (restype, argtypes)
+_vp, _u64, _i64, _i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int64, ctypes.c_int
+_ip = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "sbf_create": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64]),
+    "sbf_destroy": (None, [_vp]),
+    "sbf_insert": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "sbf_query": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "sbf_insert_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "sbf_query_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "sbf_set_host_chunk": (_i32, [_vp, _i64]),
+    "sbf_copy_bits": (_i32, [_vp, _vp, _u64, _vp]),
+    "sbf_load_bits": (_i32, [_vp, _vp, _u64, _vp]),
+    "sbf_clear": (_i32, [_vp, _vp]),
+    "sbf_num_shards": (_u64, [_vp]),
+    "sbf_get_params": (_i32, [_vp, _ip, _ip, _ip, _ip, ctypes.POINTER(ctypes.c_uint64)]),
+    "sbf_is_specialized": (_i32, [_vp]),
+    "sbf_get_status": (_i32, [_vp, _vp]),
+    "sbf_last_error": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SBFError(RuntimeError):
+    def __init__(self, code: int, where: str, message: str):
+        super().__init__(f"{where} failed ({code}): {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return build_lib.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libsbf.so (built by build_lib.build()); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or library_path()
+            if not os.path.exists(p):
+                raise ImportError(f"libsbf.so not built ({p}); run "
+                                  "minimizer_sharded_bloom_gb300.build_lib.build() first")
+            L = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    msg = load().sbf_last_error()
+    return msg.decode() if msg else ""
+
+
+def check(rc: int, where: str) -> None:
+    if rc != SBF_OK:
+        raise SBFError(rc, where, last_error())
+
+
+# ---- same-name wrappers (raw pointers as Python ints) ----------------------
+
+def sbf_create(num_bits: int, k: int, m: int, s: int, H: int, seed: int) -> int:
+    h = load().sbf_create(num_bits, k, m, s, H, seed & (2**64 - 1))
+    if not h:
+        raise SBFError(SBF_ERR_INVALID_ARG, "sbf_create", last_error())
+    return h
+
+
+def sbf_destroy(f: int) -> None:
+    load().sbf_destroy(f)
+
+
+def sbf_insert(f: int, seq: int, offsets: int, n: int, stream: int = 0) -> None:
+    check(load().sbf_insert(f, seq, offsets, n, stream), "sbf_insert")
+
+
+def sbf_query(f: int, seq: int, offsets: int, n: int, out_bits: int, stream: int = 0) -> None:
+    check(load().sbf_query(f, seq, offsets, n, out_bits, stream), "sbf_query")
+
+
+def sbf_insert_host(f: int, seq: int, offsets: int, n: int, stream: int = 0) -> None:
+    check(load().sbf_insert_host(f, seq, offsets, n, stream), "sbf_insert_host")
+
+
+def sbf_query_host(f: int, seq: int, offsets: int, n: int, out_bits: int, stream: int = 0) -> None:
+    check(load().sbf_query_host(f, seq, offsets, n, out_bits, stream), "sbf_query_host")
+
+
+def sbf_set_host_chunk(f: int, positions: int) -> None:
+    check(load().sbf_set_host_chunk(f, positions), "sbf_set_host_chunk")
+
+
+def sbf_copy_bits(f: int, dst: int, dst_bytes: int, stream: int = 0) -> None:
+    check(load().sbf_copy_bits(f, dst, dst_bytes, stream), "sbf_copy_bits")
+
+
+def sbf_load_bits(f: int, src: int, src_bytes: int, stream: int = 0) -> None:
+    check(load().sbf_load_bits(f, src, src_bytes, stream), "sbf_load_bits")
+
+
+def sbf_clear(f: int, stream: int = 0) -> None:
+    check(load().sbf_clear(f, stream), "sbf_clear")
+
+
+def sbf_num_shards(f: int) -> int:
+    return int(load().sbf_num_shards(f))
+
+
+def sbf_get_params(f: int):
+    k, m, s, H = (ctypes.c_int() for _ in range(4))
+    seed = ctypes.c_uint64()
+    check(load().sbf_get_params(f, ctypes.byref(k), ctypes.byref(m), ctypes.byref(s),
+                                ctypes.byref(H), ctypes.byref(seed)), "sbf_get_params")
+    return k.value, m.value, s.value, H.value, seed.value
+
+
+def sbf_is_specialized(f: int) -> bool:
+    return bool(load().sbf_is_specialized(f))
+
+
+def sbf_get_status(f: int, stream: int = 0) -> int:
+    return int(load().sbf_get_status(f, stream))
+
+
+def sbf_last_error() -> str:
+    return last_error()

@@ -1,0 +1,308 @@
+// sbf_api.cu -- the C ABI of libsbf (declared in include/sbf.h).
+//
+// Argument checking, filter allocation, kernel selection (compile-time
+// specialised strip kernel when one exists for (k, m, s, H), else the
+// runtime-parameter kernel) and launch.  Device-facing calls enqueue on the
+// caller's stream and return; the host-facing calls stage CSR batches through
+// pinned buffers on two streams.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "sbf_internal.h"
+#include "sbf_kernels.h"
+#include "sbf_registry.h"
+
+namespace sbf {
+extern const StripEntry kStripEntriesMain[];
+extern const int kStripCountMain;
+#ifdef SBF_WITH_SWEEP
+#define SBF_DECLARE_UNIT(M, S)                       \
+    extern const StripEntry kStripEntriesM##M##S##_[]; \
+    extern const int kStripCountM##M##S##_;
+SBF_SWEEP_UNITS(SBF_DECLARE_UNIT)
+#undef SBF_DECLARE_UNIT
+#endif
+
+bool find_specialized(int k, int m, int s, int H, const void **insert, const void **query,
+                      int *threads) {
+    struct Table {
+        const StripEntry *e;
+        const int *n;
+    };
+    static const Table tables[] = {
+        {kStripEntriesMain, &kStripCountMain},
+#ifdef SBF_WITH_SWEEP
+#define SBF_TABLE_UNIT(M, S) {kStripEntriesM##M##S##_, &kStripCountM##M##S##_},
+        SBF_SWEEP_UNITS(SBF_TABLE_UNIT)
+#undef SBF_TABLE_UNIT
+#endif
+    };
+    for (const Table &t : tables)
+        for (int i = 0; i < *t.n; ++i) {
+            const StripEntry &e = t.e[i];
+            if (e.insert && e.k == k && e.m == m && e.s == s && e.H == H) {
+                *insert = e.insert;
+                *query = e.query;
+                *threads = e.threads;
+                return true;
+            }
+        }
+    return false;
+}
+}  // namespace sbf
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int vfail(int code, const char *fmt, va_list ap) {
+    char buf[512];
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    g_last_error = buf;
+    return code;
+}
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vfail(code, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(SBF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int launch(const void *fn, int grid, int threads, const sbf::LaunchArgs &la, cudaStream_t st) {
+    sbf::LaunchArgs copy = la;
+    void *args[] = {&copy};
+    cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return SBF_OK;
+}
+
+int launch_check(const sbf_filter *f, const int64_t *offsets, int64_t n, cudaStream_t st) {
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, f->grid_check);
+    sbf::check_offsets_kernel<<<(int)std::max<int64_t>(blocks, 1), 256, 0, st>>>(offsets, n, f->status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "offsets check launch");
+    return SBF_OK;
+}
+
+sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                          uint32_t *out) {
+    sbf::LaunchArgs la;
+    la.seq = reinterpret_cast<const uint8_t *>(seq);
+    la.offsets = offsets;
+    la.n = n;
+    la.words = f->words;
+    la.out = out;
+    la.status = f->status;
+    la.shard_mask = f->num_shards - 1;
+    la.seed = f->seed;
+    la.k = f->k;
+    la.m = f->m;
+    la.s = f->s;
+    la.H = f->H;
+    return la;
+}
+
+int grid_for(const void *fn, int threads, int sms) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    return per_sm * sms;
+}
+
+int check_device(const sbf_filter *f) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != f->device)
+        return fail(SBF_ERR_INVALID_ARG, "filter lives on device %d but device %d is current", f->device, dev);
+    return SBF_OK;
+}
+
+}  // namespace
+
+int sbf::set_error(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vfail(code, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+extern "C" {
+
+const char *sbf_last_error(void) { return g_last_error.c_str(); }
+
+sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed) {
+    g_last_error.clear();
+    if (num_bits < 1) {
+        fail(SBF_ERR_INVALID_ARG, "num_bits must be >= 1");
+        return nullptr;
+    }
+    if (k < 1 || k > 32 || m < 1 || m > k || s < 1 || s > k) {
+        fail(SBF_ERR_INVALID_ARG, "need 1 <= m <= k <= 32 and 1 <= s <= k (k=%d m=%d s=%d)", k, m, s);
+        return nullptr;
+    }
+    if (H < 1 || H > 10) {
+        fail(SBF_ERR_INVALID_ARG, "H must be in 1..10 (bit-slicing needs floor(64/H) >= 6), got %d", H);
+        return nullptr;
+    }
+    const uint64_t need = num_bits / 256 + (num_bits % 256 != 0);
+    uint64_t shards = 1;
+    while (shards < need) shards <<= 1;
+    if (shards > (1ull << 40)) {
+        fail(SBF_ERR_INVALID_ARG, "filter too large: %llu shards", (unsigned long long)shards);
+        return nullptr;
+    }
+    auto *f = new sbf_filter;
+    f->k = k;
+    f->m = m;
+    f->s = s;
+    f->H = H;
+    f->seed = seed;
+    f->num_shards = shards;
+    cudaError_t e = cudaGetDevice(&f->device);
+    int sms = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, f->device);
+    if (e != cudaSuccess) {
+        cuda_fail(e, "no usable CUDA device");
+        delete f;
+        return nullptr;
+    }
+    e = cudaMalloc(reinterpret_cast<void **>(&f->words), shards * 32);
+    if (e != cudaSuccess) {
+        fail(SBF_ERR_OOM, "cudaMalloc of %llu bytes: %s", (unsigned long long)(shards * 32), cudaGetErrorString(e));
+        cudaGetLastError();
+        delete f;
+        return nullptr;
+    }
+    e = cudaMalloc(reinterpret_cast<void **>(&f->status), sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(f->words, 0, shards * 32);
+    if (e == cudaSuccess) e = cudaMemset(f->status, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        cuda_fail(e, "filter initialisation");
+        cudaFree(f->words);
+        cudaFree(f->status);
+        delete f;
+        return nullptr;
+    }
+    const void *ins = nullptr, *qry = nullptr;
+    int threads = 0;
+    // The strip kernels index shards with 32 bits.
+    if (shards <= (1ull << 32) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
+        f->specialized = true;
+    } else {
+        ins = sbf::generic_insert_kernel();
+        qry = sbf::generic_query_kernel();
+        threads = 256;
+    }
+    f->insert_kernel = ins;
+    f->query_kernel = qry;
+    f->threads = threads;
+    f->grid_insert = grid_for(ins, threads, sms);
+    f->grid_query = grid_for(qry, threads, sms);
+    f->grid_check = 4 * sms;
+    return f;
+}
+
+void sbf_destroy(sbf_filter *f) {
+    if (!f) return;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != f->device) cudaSetDevice(f->device);
+    cudaDeviceSynchronize();
+    sbf::destroy_stager(f->stager);
+    cudaFree(f->words);
+    cudaFree(f->status);
+    if (prev >= 0 && prev != f->device) cudaSetDevice(prev);
+    delete f;
+}
+
+uint64_t sbf_num_shards(const sbf_filter *f) { return f ? f->num_shards : 0; }
+
+int sbf_get_params(const sbf_filter *f, int *k, int *m, int *s, int *H, uint64_t *seed) {
+    if (!f) return fail(SBF_ERR_INVALID_ARG, "NULL filter");
+    if (k) *k = f->k;
+    if (m) *m = f->m;
+    if (s) *s = f->s;
+    if (H) *H = f->H;
+    if (seed) *seed = f->seed;
+    return SBF_OK;
+}
+
+int sbf_is_specialized(const sbf_filter *f) { return f && f->specialized ? 1 : 0; }
+
+int sbf_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream) {
+    if (!f || !seq || !offsets || n < 0) return fail(SBF_ERR_INVALID_ARG, "sbf_insert: bad arguments");
+    if (n == 0) return SBF_OK;
+    if (int rc = check_device(f)) return rc;
+    cudaStream_t st = as_stream(stream);
+    if (int rc = launch_check(f, offsets, n, st)) return rc;
+    return launch(f->insert_kernel, f->grid_insert, f->threads, make_args(f, seq, offsets, n, nullptr), st);
+}
+
+int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+              uint32_t *out_bits, void *stream) {
+    if (!f || !seq || !offsets || !out_bits || n < 0)
+        return fail(SBF_ERR_INVALID_ARG, "sbf_query: bad arguments");
+    if (n == 0) return SBF_OK;
+    if (int rc = check_device(f)) return rc;
+    cudaStream_t st = as_stream(stream);
+    if (int rc = launch_check(f, offsets, n, st)) return rc;
+    return launch(f->query_kernel, f->grid_query, f->threads, make_args(f, seq, offsets, n, out_bits), st);
+}
+
+int sbf_copy_bits(const sbf_filter *f, void *dst, uint64_t dst_bytes, void *stream) {
+    if (!f || !dst) return fail(SBF_ERR_INVALID_ARG, "sbf_copy_bits: bad arguments");
+    const uint64_t bytes = f->num_shards * 32;
+    if (dst_bytes < bytes) return fail(SBF_ERR_INVALID_ARG, "sbf_copy_bits: need %llu bytes", (unsigned long long)bytes);
+    cudaError_t e = cudaMemcpyAsync(dst, f->words, bytes, cudaMemcpyDefault, as_stream(stream));
+    return e == cudaSuccess ? SBF_OK : cuda_fail(e, "sbf_copy_bits");
+}
+
+int sbf_load_bits(sbf_filter *f, const void *src, uint64_t src_bytes, void *stream) {
+    if (!f || !src) return fail(SBF_ERR_INVALID_ARG, "sbf_load_bits: bad arguments");
+    const uint64_t bytes = f->num_shards * 32;
+    if (src_bytes != bytes) return fail(SBF_ERR_INVALID_ARG, "sbf_load_bits: need exactly %llu bytes", (unsigned long long)bytes);
+    cudaError_t e = cudaMemcpyAsync(f->words, src, bytes, cudaMemcpyDefault, as_stream(stream));
+    return e == cudaSuccess ? SBF_OK : cuda_fail(e, "sbf_load_bits");
+}
+
+int sbf_clear(sbf_filter *f, void *stream) {
+    if (!f) return fail(SBF_ERR_INVALID_ARG, "NULL filter");
+    cudaError_t e = cudaMemsetAsync(f->words, 0, f->num_shards * 32, as_stream(stream));
+    return e == cudaSuccess ? SBF_OK : cuda_fail(e, "sbf_clear");
+}
+
+int sbf_get_status(sbf_filter *f, void *stream) {
+    if (!f) return fail(SBF_ERR_INVALID_ARG, "NULL filter");
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "stream");
+    int st_word = 0;
+    e = cudaMemcpy(&st_word, f->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (st_word) {
+        e = cudaMemset(f->status, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "status clear");
+        if (st_word & sbf::kStatusBadOffsets)
+            return fail(SBF_ERR_BAD_OFFSETS, "malformed offsets (decreasing or negative); work was skipped");
+    }
+    return SBF_OK;
+}
+
+}  // extern "C"

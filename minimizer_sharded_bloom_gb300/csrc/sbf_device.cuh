@@ -1,0 +1,68 @@
+// sbf_device.cuh -- device-side definitions shared by the SBF kernels.
+//
+// The hash functions, base encoding and bit addressing of the Super Bloom
+// filter as this library fixes them ("cuSBF: A Minimizer-Aware Bloom Filter
+// for Genomic Sequence Data on Modern GPUs", Sec. IV-B, IV-C, IV-G; the
+// concrete constants and shifts are this library's reading of Sec. IV-G's
+// "single multiplicative mix" and "stronger mix with an additional xorshift").
+#pragma once
+
+#include <cstdint>
+
+namespace sbf {
+
+constexpr uint64_t kC1 = 0x9E3779B97F4A7C15ull;  // floor(2^64 / golden ratio)
+constexpr uint64_t kC2 = 0x6A09E667F3BCC909ull;  // floor((sqrt(2) - 1) * 2^64) | 1
+constexpr int kStatusBadOffsets = 1;
+
+// Everything a kernel launch needs; passed by value (kernel parameter space).
+struct LaunchArgs {
+    const uint8_t *seq;       // device bytes, readable on [offsets[0], offsets[n])
+    const int64_t *offsets;   // device CSR offsets, n + 1 entries
+    int64_t n;                // number of records
+    uint64_t *words;          // filter: num_shards * 4 words
+    uint32_t *out;            // query answer bits (absolute positions)
+    int *status;              // sticky device status word
+    uint64_t shard_mask;      // num_shards - 1
+    uint64_t seed;            // minimizer seed; the s-mer seed is ~seed
+    int k, m, s, H;
+};
+
+// Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an
+// xor-fold of the high half into the low half, whose bits pick the shard.
+__device__ __forceinline__ uint64_t hash_minimizer(uint64_t x, uint64_t seed_m) {
+    const uint64_t t = (x ^ seed_m) * kC1;
+    return t ^ (t >> 32);
+}
+
+// s-mer hash (Sec. IV-G, Bloom-bit role): stronger mix, extra xorshift.
+__device__ __forceinline__ uint64_t hash_smer(uint64_t x, uint64_t seed_s) {
+    uint64_t t = (x ^ seed_s) * kC1;
+    t ^= t >> 32;
+    t *= kC2;
+    t ^= t >> 29;
+    return t;
+}
+
+// 2-bit code of one byte, or -1: A/a 0, C/c 1, G/g 2, T/t 3 (Sec. IV-C).
+// Bits 1 and 2 of the ASCII letters give A0 C1 G3 T2; xor-ing bit 1 into bit 0
+// of that pair gives A0 C1 G2 T3.  Validity: the byte's top bits are 01x and its
+// low five bits are 1 (A), 3 (C), 7 (G) or 20 (T).
+__device__ __forceinline__ int base_code(uint32_t c) {
+    const bool ok = ((c & 0xC0u) == 0x40u) && ((0x0010008Au >> (c & 31u)) & 1u);
+    const int code = (int)(((c >> 1) ^ (c >> 2)) & 3u);
+    return ok ? code : -1;
+}
+
+// OR the H bits of one s-mer hash into four word masks (Sec. IV-B: hash i ->
+// word i mod 4; Sec. IV-G: bit-slicing with slice width floor(64/H)).
+__device__ __forceinline__ void smer_bits_runtime(uint64_t hs, int H, uint64_t K[4]) {
+    const int W = 64 / H;
+    for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);
+}
+
+__device__ __forceinline__ uint64_t low_mask(int symbols) {
+    return symbols >= 32 ? ~0ull : ((1ull << (2 * symbols)) - 1ull);
+}
+
+}  // namespace sbf

@@ -1,0 +1,6 @@
+// Sweep-grid specialisations for k = 31, m = 16, s = 31, H in {1, 2, 4, 6, 8}.
+#include "sbf_registry.h"
+
+namespace sbf {
+SBF_REGISTER_MS(16, 31)
+}  // namespace sbf

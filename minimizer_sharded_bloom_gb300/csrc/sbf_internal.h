@@ -1,0 +1,29 @@
+// sbf_internal.h -- the filter object and helpers shared by the C ABI units.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/sbf.h"
+
+struct sbf_filter {
+    int device = 0;
+    int k = 0, m = 0, s = 0, H = 0;
+    uint64_t seed = 0;
+    uint64_t num_shards = 0;
+    uint64_t *words = nullptr;  // num_shards * 4 words
+    int *status = nullptr;      // sticky device status
+    const void *insert_kernel = nullptr;
+    const void *query_kernel = nullptr;
+    int threads = 256;
+    int grid_insert = 0, grid_query = 0;
+    int grid_check = 0;
+    bool specialized = false;
+    void *stager = nullptr;     // host-facing staging buffers, created on first use
+    int64_t host_chunk = int64_t(1) << 27;  // host-facing chunk, in positions
+};
+
+namespace sbf {
+// Records the calling thread's error message and returns `code`.
+int set_error(int code, const char *fmt, ...);
+void destroy_stager(void *stager);
+}  // namespace sbf

@@ -34,19 +34,31 @@ def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
 
+_CHUNK = 1 << 26
+
+
 def uniform_bases(rng: np.random.Generator, n: int) -> np.ndarray:
-    return ACGT[rng.integers(0, 4, size=n, dtype=np.uint8)]
+    """n i.i.d. uniform bases over ACGT (drawn in chunks of 2^26)."""
+    out = np.empty(n, dtype=np.uint8)
+    for c in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - c)
+        out[c:c + m] = ACGT[rng.integers(0, 4, size=m, dtype=np.uint8)]
+    return out
 
 
 def substitute(rng: np.random.Generator, seq: np.ndarray, rate: float) -> np.ndarray:
     """Each base independently, with probability `rate`, becomes one of the
-    other three bases, chosen uniformly.  Returns a new array."""
+    other three bases, chosen uniformly.  Returns a new array (chunks of
+    2^26 bases: a uniform draw per base, then a uniform shift of 1..3 for the
+    hit ones)."""
     out = seq.copy()
-    hit = np.flatnonzero(rng.random(seq.size) < rate)
-    if hit.size:
-        idx = np.searchsorted(ACGT, out[hit])  # ACGT is sorted: A<C<G<T
-        shift = rng.integers(1, 4, size=hit.size)
-        out[hit] = ACGT[(idx + shift) % 4]
+    for c in range(0, seq.size, _CHUNK):
+        part = out[c:c + _CHUNK]
+        hit = np.flatnonzero(rng.random(part.size) < rate)
+        if hit.size:
+            idx = np.searchsorted(ACGT, part[hit])  # ACGT is sorted: A<C<G<T
+            shift = rng.integers(1, 4, size=hit.size)
+            part[hit] = ACGT[(idx + shift) % 4]
     return out
 
 

@@ -72,6 +72,11 @@ def lib() -> ctypes.CDLL:
             L.orc_kmer_info.restype = i32
             L.orc_count_runs.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, vp, vp, vp]
             L.orc_count_runs.restype = i32
+            L.orc_kmer_batch.argtypes = [vp, vp, i64, vp, i64, i32, i32, i32, i32, u64, u64,
+                                         vp, vp, vp]
+            L.orc_kmer_batch.restype = i32
+            L.orc_kmer_rows.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, vp, vp, vp]
+            L.orc_kmer_rows.restype = i32
             _lib = L
     return _lib
 
@@ -184,3 +189,58 @@ def smer_bits(hs: int, H: int):
 def constants():
     L = lib()
     return int(L.orc_const_c1()), int(L.orc_const_c2())
+
+
+def kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed):
+    """(valid[bool], shard[uint64], K[uint64, 4]) for each absolute position."""
+    a, o = _u8(seq), _i64(offsets)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    valid = np.zeros(pos.size, dtype=np.uint8)
+    shard = np.zeros(pos.size, dtype=np.uint64)
+    K = np.zeros((pos.size, 4), dtype=np.uint64)
+    if pos.size:
+        rc = lib().orc_kmer_batch(_ptr(a), _ptr(o), o.size - 1, _ptr(pos), pos.size, k, m, s, H,
+                                  num_shards, seed & (2**64 - 1), _ptr(valid), _ptr(shard), _ptr(K))
+        if rc != 0:
+            raise ValueError("orc_kmer_batch rejected its arguments")
+    return valid.astype(bool), shard, K
+
+
+def query_sampled(shard_words, seq, offsets, positions, k, m, s, H, num_shards, seed):
+    """Answers for selected absolute positions only, for filters too large to
+    copy whole.  shard_words(uint64 array of shards) -> uint64[len, 4] supplies
+    the image words of the requested shards.  Each answer follows Algorithm 2:
+    present iff the k-mer is valid and every bit of its s-mers is set in its
+    shard."""
+    valid, shard, K = kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed)
+    out = np.zeros(valid.size, dtype=bool)
+    if valid.any():
+        F = np.asarray(shard_words(shard[valid]), dtype=np.uint64).reshape(-1, 4)
+        out[valid] = ((K[valid] & ~F) == 0).all(axis=1)
+    return out
+
+
+def insert_sparse(seq, offsets, k, m, s, H, num_shards, seed):
+    """The image a full insert produces, as (sorted non-zero shard indices,
+    uint64[len, 4] words), without allocating num_shards rows: every valid
+    k-mer's (shard, K) from scratch, then an OR per shard (a sort and a
+    segmented OR-reduce)."""
+    a, o = _u8(seq), _i64(offsets)
+    total = int(np.maximum(np.diff(o), 0).sum())
+    shard = np.zeros(max(total, 1), dtype=np.uint64)
+    K = np.zeros((max(total, 1), 4), dtype=np.uint64)
+    cnt = np.zeros(1, dtype=np.int64)
+    rc = lib().orc_kmer_rows(_ptr(a), _ptr(o), o.size - 1, k, m, s, H, num_shards,
+                             seed & (2**64 - 1), _ptr(shard), _ptr(K), _ptr(cnt))
+    if rc != 0:
+        raise ValueError("orc_kmer_rows rejected its arguments")
+    c = int(cnt[0])
+    shard, K = shard[:c], K[:c]
+    order = np.argsort(shard, kind="stable")
+    shard, K = shard[order], K[order]
+    if c == 0:
+        return shard, K
+    starts = np.flatnonzero(np.concatenate([[True], shard[1:] != shard[:-1]]))
+    words = np.bitwise_or.reduceat(K, starts, axis=0)
+    keep = words.any(axis=1)
+    return shard[starts][keep], words[keep]

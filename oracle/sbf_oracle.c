@@ -371,3 +371,48 @@ int orc_count_runs(const uint8_t *seq, const int64_t *off, int64_t n,
     *atomics = na;
     return 0;
 }
+
+/* Per-position evaluation for sampled checks on inputs too large for a full
+ * oracle pass: for each absolute position pos[i] (any order), valid[i],
+ * shard[i] and K[4i..4i+3] as kmer_info computes them.  Positions outside
+ * [off[0], off[n]) are reported invalid.  Returns 0, or -1 on bad
+ * arguments. */
+int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
+                   const int64_t *pos, int64_t count,
+                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                   uint8_t *valid, uint64_t *shard, uint64_t *K)
+{
+    orc_params P = {k, m, s, H, num_shards, seed};
+    if (!valid_params(&P) || n <= 0)
+        return -1;
+    for (int64_t i = 0; i < count; i++) {
+        int64_t g = pos[i];
+        valid[i] = 0;
+        shard[i] = 0;
+        K[4 * i] = K[4 * i + 1] = K[4 * i + 2] = K[4 * i + 3] = 0;
+        if (g < off[0] || g >= off[n])
+            continue;
+        int64_t r = record_of(off, n, g);
+        valid[i] = (uint8_t)kmer_info(seq, g, off[r + 1], &P, &shard[i], &K[4 * i]);
+    }
+    return 0;
+}
+
+/* Every valid k-mer as (shard, K) rows, in position order, for building a
+ * sparse image.  rows must hold one entry per k-mer position; *count
+ * receives the number of valid k-mers written. */
+int orc_kmer_rows(const uint8_t *seq, const int64_t *off, int64_t n,
+                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                  uint64_t *shard, uint64_t *K, int64_t *count)
+{
+    orc_params P = {k, m, s, H, num_shards, seed};
+    if (!valid_params(&P) || !check_offsets(off, n))
+        return -1;
+    int64_t c = 0;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t g = off[r]; g < off[r + 1]; g++)
+            if (kmer_info(seq, g, off[r + 1], &P, &shard[c], &K[4 * c]))
+                c++;
+    *count = c;
+    return 0;
+}

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry
+point include/sbf.h declares; the binding covers exactly those names.  No
+compute call is made here."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sbf.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sbf_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not shutil.which("nvcc") and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from minimizer_sharded_bloom_gb300 import build_lib
+    path = build_lib.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("sbf_create", "sbf_insert", "sbf_query", "sbf_copy_bits", "sbf_destroy",
+                     "sbf_get_status", "sbf_last_error", "sbf_insert_host", "sbf_query_host"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_matches_header():
+    from minimizer_sharded_bloom_gb300 import _native
+    assert sorted(_native.SIGNATURES) == declared_functions()
+    for name in declared_functions():
+        assert callable(getattr(_native, name))
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from minimizer_sharded_bloom_gb300 import _native
+    with pytest.raises(ImportError):
+        _native._lib = None
+        try:
+            _native.load(str(tmp_path / "missing.so"))
+        finally:
+            _native._lib = None
+
+
+def test_argument_errors_need_no_gpu(lib):
+    """Host-side validation returns SBF_ERR_INVALID_ARG before touching CUDA."""
+    from minimizer_sharded_bloom_gb300 import _native
+    L = _native.load()
+    assert not L.sbf_create(0, 31, 16, 28, 4, 0)
+    assert "num_bits" in _native.last_error()
+    assert not L.sbf_create(1 << 20, 33, 16, 28, 4, 0)
+    assert not L.sbf_create(1 << 20, 31, 16, 28, 11, 0)
+    assert not L.sbf_create(1 << 20, 31, 32, 28, 4, 0)
+    assert L.sbf_insert(None, None, None, 1, None) == _native.SBF_ERR_INVALID_ARG
+    assert L.sbf_query(None, None, None, 1, None, None) == _native.SBF_ERR_INVALID_ARG
+    assert L.sbf_num_shards(None) == 0
+    L.sbf_destroy(None)
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    """On a machine without a CUDA device creation reports an error (no CPU
+    fallback, no crash)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from minimizer_sharded_bloom_gb300 import _native
+    L = _native.load()
+    assert not L.sbf_create(1 << 20, 31, 16, 28, 4, 0)
+    assert _native.last_error()

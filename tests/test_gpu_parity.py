@@ -1,0 +1,239 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle: bit-exact
+filter images and answer bits, on seeded inputs that span several tiles with a
+ragged tail, over the specialised and the runtime-parameter kernels, and on the
+edge cases of the contract."""
+import numpy as np
+import pytest
+
+import oracle
+from minimizer_sharded_bloom_gb300 import synth
+from _gpu_helpers import (MAIN, assert_images_equal, assert_words_equal, gpu_insert, gpu_query,
+                          need_gpu, oracle_answers, oracle_image, to_dev, answer_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return need_gpu()
+
+
+def _filter(num_bits, params, seed):
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter
+    return SuperBloomFilter(num_bits, seed=seed, **params)
+
+
+def _roundtrip(torch, ins, qry, params, num_bits, seed, pad_front=0, expect_specialized=None):
+    sbf = _filter(num_bits, params, seed)
+    if expect_specialized is not None:
+        assert sbf.specialized == expect_specialized
+    gpu_insert(torch, sbf, ins.seq, ins.offsets, pad_front)
+    F = oracle_image(ins.seq, ins.offsets, params, num_bits, seed)
+    assert_images_equal(sbf.to_numpy(), F)
+    got = gpu_query(torch, sbf, qry.seq, qry.offsets, pad_front)
+    want = oracle_answers(F, qry.seq, qry.offsets, params, seed)
+    assert_words_equal(got, want, qry.offsets)
+    sbf.close()
+    return F, got
+
+
+def test_tiny_config(torch):
+    """tiny: 100 kbp into 2^20 bits; the inserted record answers all-positive,
+    the independent one measures the false-positive rate."""
+    ins, qry = synth.tiny()
+    F, got = _roundtrip(torch, ins, qry, MAIN, 1 << 20, seed=1, expect_specialized=True)
+    first = np.arange(0, 100_000 - 31 + 1)
+    assert answer_bits(got, first).all()
+    second = np.arange(100_000, 200_000 - 31 + 1)
+    fpr = answer_bits(got, second).mean()
+    assert fpr < 0.05
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_main_config_mixed_records(torch, case):
+    """k=31,m=16,s=28,H=4 (specialised kernel) on mixed records: N runs,
+    lowercase, junk bytes, empty and short records, several tiles, ragged
+    tail, and an unaligned sequence pointer for odd cases."""
+    rng = np.random.default_rng(500 + case)
+    ins = synth.random_records(rng, int(rng.integers(1, 60)), 0, int(rng.integers(40, 20000)),
+                               n_prob=0.002 * (case % 3), lower_prob=0.05 * (case % 2),
+                               junk_prob=0.0005 * (case % 4 == 3))
+    qry = synth.random_records(rng, int(rng.integers(1, 200)), 0, 400, n_prob=0.001)
+    qry = synth.Workload(np.concatenate([ins.seq, qry.seq]),
+                         np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]]))
+    bits = int(1 << int(rng.integers(10, 22)))
+    _roundtrip(torch, ins, qry, MAIN, bits, seed=int(rng.integers(0, 2**62)),
+               pad_front=(case * 5) % 16, expect_specialized=True)
+
+
+GRID = [(m, s, H) for m in (12, 14, 16, 18, 21) for s in (20, 24, 28, 31) for H in (1, 2, 4, 6, 8)]
+
+
+@pytest.mark.parametrize("m,s,H", GRID)
+def test_sweep_grid_specialisations(torch, m, s, H):
+    """Every (s, m, H) of the k = 31 sweep grid runs its own specialised
+    kernel; each must match the oracle bit for bit."""
+    rng = np.random.default_rng(1000 + 100 * m + 10 * s + H)
+    params = dict(k=31, m=m, s=s, H=H)
+    ins = synth.random_records(rng, 3, 10_000, 25_000, n_prob=0.0005)
+    q_rand = synth.Workload(synth.uniform_bases(rng, 3000 * 31), synth.csr(np.full(3000, 31)))
+    qry = synth.Workload(np.concatenate([ins.seq, q_rand.seq]),
+                         np.concatenate([ins.offsets, ins.offsets[-1] + q_rand.offsets[1:]]))
+    _roundtrip(torch, ins, qry, params, 1 << 16, seed=77 + H, expect_specialized=True)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_runtime_parameter_kernel(torch, case):
+    """(k, m, s, H) outside the specialised grid run the runtime-parameter
+    kernel, which must match the oracle too."""
+    rng = np.random.default_rng(2000 + case)
+    while True:
+        k = int(rng.integers(1, 33))
+        m = int(rng.integers(1, k + 1))
+        s = int(rng.integers(1, k + 1))
+        H = int(rng.integers(1, 11))
+        if not (k == 31 and m in (12, 14, 16, 18, 21) and s in (20, 24, 28, 31) and H in (1, 2, 4, 6, 8)):
+            break
+    params = dict(k=k, m=m, s=s, H=H)
+    ins = synth.random_records(rng, int(rng.integers(1, 30)), 0, 3000, n_prob=0.01, lower_prob=0.1)
+    qry = synth.random_records(rng, int(rng.integers(1, 30)), 0, 300, n_prob=0.01)
+    qry = synth.Workload(np.concatenate([ins.seq, qry.seq]),
+                         np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]]))
+    _roundtrip(torch, ins, qry, params, 1 << int(rng.integers(8, 16)), seed=case * 977,
+               pad_front=case % 7, expect_specialized=False)
+
+
+def test_edge_cases(torch):
+    """Records of length 0, k-1, k, k+1 and 31 + 32 j; an all-N record; a
+    first record that does not start at 0; a single base."""
+    k = 31
+    texts = ["", "A" * (k - 1), "ACGT" * 7 + "ACG", "C" * (k + 1), "N" * 100, "G"]
+    rng = np.random.default_rng(3)
+    texts += ["".join(rng.choice(list("ACGT"), size=31 + 32 * j)) for j in range(1, 5)]
+    seq = np.frombuffer("".join(texts).encode(), dtype=np.uint8).copy()
+    off = synth.csr([len(t) for t in texts])
+    ins = synth.Workload(seq, off)
+    _roundtrip(torch, ins, ins, MAIN, 1 << 12, seed=5)
+    # the same records shifted so that offsets[0] = 37 (bytes before it unused)
+    seq2 = np.concatenate([np.full(37, ord("T"), dtype=np.uint8), seq])
+    ins2 = synth.Workload(seq2, off + 37)
+    _roundtrip(torch, ins2, ins2, MAIN, 1 << 12, seed=5)
+
+
+def test_empty_batch_is_a_noop(torch):
+    sbf = _filter(1 << 12, MAIN, 1)
+    seq, off = to_dev(torch, np.zeros(0, np.uint8), np.zeros(1, np.int64))
+    sbf.insert(seq, off)
+    out = torch.full((4,), 7, dtype=torch.int32, device="cuda")
+    sbf.query(seq, off, out=out)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy() == 7).all()
+    assert not sbf.to_numpy().any()
+    assert sbf.status() == 0
+
+
+def test_query_writes_exactly_the_contract_words(torch):
+    """Words in [offsets[0] >> 5, (offsets[n] + 31) >> 5) are written, the
+    rest are left alone."""
+    rng = np.random.default_rng(9)
+    body = synth.uniform_bases(rng, 5000)
+    seq = np.concatenate([np.full(100, ord("A"), np.uint8), body])
+    off = np.array([100, 2100, 5100], dtype=np.int64)
+    sbf = _filter(1 << 14, MAIN, 4)
+    gpu_insert(torch, sbf, seq, off)
+    got = gpu_query(torch, sbf, seq, off, sentinel=-1)
+    lo, hi = 100 >> 5, (5100 + 31) >> 5
+    assert (got[:lo] == 0xFFFFFFFF).all() and (got[hi:] == 0xFFFFFFFF).all()
+    F = oracle_image(seq, off, MAIN, 1 << 14, 4)
+    assert_words_equal(got, oracle_answers(F, seq, off, MAIN, 4), off)
+
+
+def test_bad_offsets_set_the_status(torch):
+    """Decreasing offsets: the device check sets the sticky status, the
+    kernels skip the work, sbf_get_status reports and clears it."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(10)
+    seq = synth.uniform_bases(rng, 4000)
+    good = np.array([0, 2000, 4000], dtype=np.int64)
+    bad = np.array([0, 3000, 2000, 4000], dtype=np.int64)
+    sbf = _filter(1 << 14, MAIN, 4)
+    dseq, doff = to_dev(torch, seq, bad)
+    sbf.insert(dseq, doff)
+    assert sbf.status() == N.SBF_ERR_BAD_OFFSETS
+    assert not sbf.to_numpy().any()
+    assert sbf.status() == 0
+    gpu_insert(torch, sbf, seq, good)
+    assert sbf.status() == 0
+    assert_images_equal(sbf.to_numpy(), oracle_image(seq, good, MAIN, 1 << 14, 4))
+
+
+def test_filter_algebra_on_gpu(torch):
+    """Order independence, split inserts, idempotence and union, on the GPU
+    image (OR is commutative and idempotent)."""
+    rng = np.random.default_rng(11)
+    a = synth.random_records(rng, 40, 100, 3000, n_prob=0.001)
+    b = synth.random_records(rng, 40, 100, 3000, n_prob=0.001)
+    both = synth.Workload(np.concatenate([b.seq, a.seq]),
+                          np.concatenate([b.offsets, b.offsets[-1] + a.offsets[1:]]))
+    bits = 1 << 16
+    fa = gpu_insert(torch, _filter(bits, MAIN, 8), a.seq, a.offsets).to_numpy()
+    fb = gpu_insert(torch, _filter(bits, MAIN, 8), b.seq, b.offsets).to_numpy()
+    s = _filter(bits, MAIN, 8)
+    gpu_insert(torch, s, both.seq, both.offsets)
+    fab = s.to_numpy()
+    assert np.array_equal(fab, fa | fb)
+    gpu_insert(torch, s, a.seq, a.offsets)
+    assert np.array_equal(s.to_numpy(), fab)
+
+
+def test_copy_load_clear(torch):
+    rng = np.random.default_rng(12)
+    a = synth.random_records(rng, 10, 1000, 5000)
+    s1 = gpu_insert(torch, _filter(1 << 15, MAIN, 3), a.seq, a.offsets)
+    img = s1.to_numpy()
+    s2 = _filter(1 << 15, MAIN, 3)
+    s2.load(img)
+    assert np.array_equal(s2.to_numpy(), img)
+    assert np.array_equal(gpu_query(torch, s1, a.seq, a.offsets), gpu_query(torch, s2, a.seq, a.offsets))
+    dev = s1.to_tensor()
+    s3 = _filter(1 << 15, MAIN, 3)
+    s3.load(dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(s3.to_numpy(), img)
+    s2.clear()
+    torch.cuda.synchronize()
+    assert not s2.to_numpy().any()
+
+
+@pytest.mark.parametrize("pinned", [False, True])
+@pytest.mark.parametrize("params", [MAIN, dict(k=25, m=11, s=20, H=3)])
+def test_host_entry_points(torch, pinned, params):
+    """sbf_insert_host / sbf_query_host, chunked at 4096 positions so that
+    records and k-mers straddle chunk edges, with pageable and pinned host
+    buffers, equal the oracle."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(13)
+    ins = synth.random_records(rng, 30, 0, 2500, n_prob=0.002)
+    qry = synth.random_records(rng, 50, 0, 900, n_prob=0.002)
+    qry = synth.Workload(np.concatenate([ins.seq, qry.seq]),
+                         np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]]))
+    sbf = _filter(1 << 14, params, 21)
+    N.sbf_set_host_chunk(sbf.handle, 4096)
+    if pinned:
+        def pin(a):
+            t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+            return t, t.numpy()
+        _ks, s_ins = pin(ins.seq)
+        _ko, o_ins = pin(ins.offsets)
+        _kq, s_q = pin(qry.seq)
+        _kqo, o_q = pin(qry.offsets)
+        out_t = torch.zeros((int(qry.offsets[-1]) + 31) // 32 + 1, dtype=torch.int32).pin_memory()
+        out = out_t.numpy().view(np.uint32)
+    else:
+        s_ins, o_ins, s_q, o_q = ins.seq, ins.offsets, qry.seq, qry.offsets
+        out = np.zeros((int(qry.offsets[-1]) + 31) // 32 + 1, dtype=np.uint32)
+    sbf.insert_host(s_ins, o_ins)
+    F = oracle_image(ins.seq, ins.offsets, params, 1 << 14, 21)
+    assert_images_equal(sbf.to_numpy(), F)
+    sbf.query_host(s_q, o_q, out=out)
+    assert_words_equal(out, oracle_answers(F, qry.seq, qry.offsets, params, 21), qry.offsets)
