@@ -112,6 +112,25 @@ int sbf_insert_host(sbf_filter *f, const char *seq, const int64_t *offsets, int6
 int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                    uint32_t *out_bits, void *stream);
 
+/* Host-facing query that allocates nothing (the paper has no counterpart).
+ * For callers that cannot allocate device memory at call time -- code running
+ * under an allocator that owns the whole device (a framework's caching
+ * allocator, a fixed memory budget), or loops that cannot accept the implicit
+ * device synchronisation of cudaMalloc/cudaFree.  Same inputs, outputs and
+ * results as sbf_query_host (HOST seq/offsets/out_bits, same layout), but the
+ * batch is staged through one fixed device array that the library holds on
+ * every device that loads it until the process exits (about 26 MiB).
+ * Limits: offsets[n] - offsets[0] <= 2^24 positions and n <= 2^20 records;
+ * larger batches fail with SBF_ERR_INVALID_ARG and nothing is copied.  Calls
+ * no cudaMalloc/cudaFree or any other allocating routine.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * All calls share the array: calls whose work overlaps on the GPU (e.g. on two
+ * streams) race.  Work is ordered on `stream`; returns when out_bits is
+ * complete. */
+int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                           uint32_t *out_bits, void *stream);
+
 /* Chunk size of the host-facing calls, in sequence positions (default 2^27;
  * rounded down to a multiple of 32; at least 32).  Smaller chunks overlap
  * copies and kernels at a finer grain and need smaller staging buffers. */

@@ -27,6 +27,7 @@ SIGNATURES = {
     "sbf_query": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "sbf_insert_host": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "sbf_query_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "sbf_query_host_noalloc": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "sbf_set_host_chunk": (_i32, [_vp, _i64]),
     "sbf_copy_bits": (_i32, [_vp, _vp, _u64, _vp]),
     "sbf_load_bits": (_i32, [_vp, _vp, _u64, _vp]),
@@ -107,6 +108,12 @@ def sbf_insert_host(f: int, seq: int, offsets: int, n: int, stream: int = 0) -> 
 
 def sbf_query_host(f: int, seq: int, offsets: int, n: int, out_bits: int, stream: int = 0) -> None:
     check(load().sbf_query_host(f, seq, offsets, n, out_bits, stream), "sbf_query_host")
+
+
+def sbf_query_host_noalloc(f: int, seq: int, offsets: int, n: int, out_bits: int,
+                           stream: int = 0) -> None:
+    check(load().sbf_query_host_noalloc(f, seq, offsets, n, out_bits, stream),
+          "sbf_query_host_noalloc")
 
 
 def sbf_set_host_chunk(f: int, positions: int) -> None:
