@@ -47,6 +47,10 @@ WORKLOADS = {
                          desc="out-of-cache: 1 Gbp in 10,000 log-normal contigs (median 50 kbp) "
                               "into a 2^36-bit (8 GiB) filter; query 6,666,666 x 150 bp reads "
                               "(50% from the contigs at 1% error, 50% uniform)"),
+    "out-of-cache-small": dict(bits=1 << 34, make=lambda: synth.out_of_cache(total=200_000_000,
+                                                                               n_contigs=2_000),
+                               desc="out-of-cache, profiling size: 200 Mbp in 2,000 log-normal contigs "
+                                    "into a 2^34-bit (2 GiB) filter; query 1,333,333 x 150 bp reads"),
     "genome-like": dict(bits=1 << 30, make=lambda: synth.genome_like(),
                         desc="genome-like: 50 Mbp with 20% copied 1-10 kbp segments at 1% error "
                              "into a 2^30-bit (128 MiB) filter; query 1,000,000 x 150 bp reads"),
@@ -57,16 +61,22 @@ WORKLOADS = {
                  desc="tiny: 100 kbp into 2^20 bits; query it plus 100 kbp uniform"),
 }
 
-# Algorithmic 32-bit integer operations per k-mer of the rolling formulation
-# (k=31, m=16, s=28, H=4), counted in the design notes: shared front end 50
-# (decode 1, validity 1, m-mer roll 1, s-mer roll 2, minimizer hash 5,
-# 3 sliding-window 64-bit minimums 12, shard 1, s-mer hash 15, four bit
-# positions to one-hot word halves 12); insert adds 10 (run compare, select,
-# OR of the new s-mer into the run's eight half-words); query adds 26 (k-mer
-# mask from four s-mer masks 16, subset test 9, answer bit 1).
-ALU_OPS_PER_KMER = {"insert": 60, "query": 76}
-# Integer peak: 152 SMs x 128 INT32 lanes x 2.07 GHz maximum SM clock.
-ALU_PEAK_TOPS = 152 * 128 * 2.07e9 / 1e12
+# Algorithmic integer operations per k-mer of the rolling formulation
+# (k=31, m=16, s=28, H=4) that run on the ALU pipe (logic, shift, compare,
+# select), counted in the design notes: shared front end 39 (decode 1,
+# validity 1, m-mer and s-mer extraction 3, minimizer-hash xor + fold 2,
+# three 64-bit sliding-window minimums 12, shard 1, s-mer-hash xors and
+# xorshifts 7, four bit positions to one-hot word halves 12); insert adds 10
+# (run compare, select, OR of the newest s-mer into the run's eight
+# half-words); query adds 26 (k-mer mask from four s-mer masks 16, subset test
+# 9, answer bit 1).  The multiplies of the two hashes (11 per k-mer) run on
+# the FMA pipe and are not counted.
+ALU_OPS_PER_KMER = {"insert": 49, "query": 65}
+# ALU-pipe peak: 152 SMs x 4 sub-partitions x 16 lanes x 2.07 GHz (maximum SM
+# clock).  ncu reports the ALU pipe at 16 lanes per sub-partition: with the
+# pipe ~75 % busy the issue rate is ~53 %, i.e. one ALU warp-instruction per
+# two cycles at most.
+ALU_PEAK_TOPS = 152 * 64 * 2.07e9 / 1e12
 
 # ncu DRAM bytes (read + write) per k-mer of the out-of-cache launches, valid
 # only for the kernel source they were measured on.
@@ -274,6 +284,7 @@ def main():
         N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
         N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), n_q, out.data_ptr(), sh)
 
+    rmw_ceiling = random_rmw_ceiling(torch) if args.workload.startswith("out-of-cache") else None
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -313,32 +324,45 @@ def main():
     fpr = fpr_of(words, qry)
     value = world * args.steps * (nk_ins + nk_q) / total
 
-    # roofline of the dominant kernel (the longer of insert and query)
+    # rooflines: insert against HBM (one 32-byte sector read and written per
+    # run), query against the ALU pipe; "roofline" is the dominant (longer) one.
     peaks, peak_src = measured_peaks()
     avg_ins, avg_q = s_ins / args.steps, s_q / args.steps
-    dom = "insert" if avg_ins >= avg_q else "query"
-    dom_t = max(avg_ins, avg_q)
-    dom_k = nk_ins if dom == "insert" else nk_q
-    alu_ach = ALU_OPS_PER_KMER[dom] * dom_k / dom_t / 1e12
     sha = kernel_source_sha()
-    traffic = None
-    if MEASURED_TRAFFIC["source_sha"] == sha and MEASURED_TRAFFIC[dom] is not None \
-            and args.workload == "out-of-cache":
-        traffic = MEASURED_TRAFFIC[dom] * dom_k
-    roofline = {"bound": "alu", "kernel": f"strip_kernel<31,16,28,4,{dom}>",
-                "achieved": alu_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (int32)",
-                "frac": alu_ach / ALU_PEAK_TOPS, "traffic": traffic,
-                "peak_source": "152 SMs x 128 INT32 lanes x 2.07 GHz (recipe unit counts)",
-                "ops_per_kmer": ALU_OPS_PER_KMER[dom], "avg_launch_ms": 1e3 * dom_t}
     runs_i, runs_q = runs_estimate(ins), runs_estimate(qry)
     bytes_ins = ins.n_bases + 8 * (n_ins + 1) + 64 * runs_i
     bytes_q = qry.n_bases + 8 * (n_q + 1) + 32 * runs_q + 4 * ((qry.n_bases + 31) // 32)
-    hbm = {}
-    for name, b, t in (("insert", bytes_ins, avg_ins), ("query", bytes_q, avg_q)):
-        ach = b / t / 1e9
-        hbm[name] = {"achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
-                     "algorithmic_bytes_per_kmer": b / (nk_ins if name == "insert" else nk_q),
-                     "peak_source": f"{peak_src} hbm_gbs"}
+
+    def traffic_of(name, nk):
+        if (MEASURED_TRAFFIC["source_sha"] == sha and MEASURED_TRAFFIC[name] is not None
+                and args.workload == "out-of-cache"):
+            return MEASURED_TRAFFIC[name] * nk
+        return None
+
+    ins_ach = bytes_ins / avg_ins / 1e9
+    roof_ins = {"bound": "hbm", "kernel": "strip_kernel<31,16,28,4,insert>",
+                "achieved": ins_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ins_ach / peaks["hbm_gbs"], "traffic": traffic_of("insert", nk_ins),
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_kmer": bytes_ins / nk_ins,
+                "runs_per_launch": runs_i, "avg_launch_ms": 1e3 * avg_ins}
+    if rmw_ceiling:
+        roof_ins["pattern_peak"] = {
+            "what": "random 32-byte row read-modify-write (4 x 64-bit atomic add per row, "
+                    "torch index_add_) over an 8 GiB tensor, measured in this run",
+            "rows_per_s": rmw_ceiling, "runs_per_s": runs_i / avg_ins,
+            "frac": runs_i / avg_ins / rmw_ceiling}
+    q_ach = ALU_OPS_PER_KMER["query"] * nk_q / avg_q / 1e12
+    roof_q = {"bound": "alu", "kernel": "strip_kernel<31,16,28,4,query>",
+              "achieved": q_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (ALU pipe)",
+              "frac": q_ach / ALU_PEAK_TOPS, "traffic": traffic_of("query", nk_q),
+              "peak_source": "152 SMs x 64 ALU lanes x 2.07 GHz (recipe SM count and clock)",
+              "ops_per_kmer": ALU_OPS_PER_KMER["query"], "avg_launch_ms": 1e3 * avg_q,
+              "algorithmic_bytes_per_kmer": bytes_q / nk_q,
+              "hbm_frac": bytes_q / avg_q / 1e9 / peaks["hbm_gbs"]}
+    ins_alu = ALU_OPS_PER_KMER["insert"] * nk_ins / avg_ins / 1e12
+    roof_ins["alu_frac"] = ins_alu / ALU_PEAK_TOPS
+    roofline, roofline_other = (roof_ins, roof_q) if avg_ins >= avg_q else (roof_q, roof_ins)
 
     e2e = None
     if not args.no_e2e:
@@ -365,7 +389,7 @@ def main():
             "insert_kmers_per_s": world * args.steps * nk_ins / s_ins,
             "query_kmers_per_s": world * args.steps * nk_q / s_q,
             "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
-            "roofline": roofline, "roofline_hbm": hbm,
+            "roofline": roofline, "roofline_other_kernel": roofline_other,
             "gpu_launches": 4 * args.steps,
             "gpu_launches_note": "per step: offsets check + strip kernel for insert and for query",
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cb,
@@ -375,6 +399,30 @@ def main():
     sbf.close()
     if pg:
         pg.destroy_process_group()
+
+
+def random_rmw_ceiling(torch, gib: int = 8, rows_touched: int = 25_000_000) -> float:
+    """Rows per second of random 32-byte read-modify-writes over a gib-GiB
+    tensor (torch index_add_: four 64-bit atomic adds per row) -- the memory
+    system's ceiling for the insert's per-run shard update."""
+    n_rows = (gib << 30) // 32
+    F = torch.zeros(n_rows, 4, dtype=torch.int64, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(1)
+    idx = torch.randint(0, n_rows, (rows_touched,), device="cuda", generator=g)
+    src = torch.ones(rows_touched, 4, dtype=torch.int64, device="cuda")
+    for _ in range(2):
+        F.index_add_(0, idx, src)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        F.index_add_(0, idx, src)
+    e1.record()
+    torch.cuda.synchronize()
+    rate = 3 * rows_touched / (e0.elapsed_time(e1) / 1e3)
+    del F, idx, src
+    torch.cuda.empty_cache()
+    return rate
 
 
 def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):

@@ -202,8 +202,8 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
     }
     const void *ins = nullptr, *qry = nullptr;
     int threads = 0;
-    // The strip kernels index shards with 32 bits.
-    if (shards <= (1ull << 32) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
+    // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
+    if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
     } else {
         ins = sbf::generic_insert_kernel();
@@ -301,6 +301,8 @@ int sbf_get_status(sbf_filter *f, void *stream) {
         if (e != cudaSuccess) return cuda_fail(e, "status clear");
         if (st_word & sbf::kStatusBadOffsets)
             return fail(SBF_ERR_BAD_OFFSETS, "malformed offsets (decreasing or negative); work was skipped");
+        if (st_word & sbf::kStatusTimeout)
+            return fail(SBF_ERR_CUDA, "a bounded device wait timed out; the call's work is incomplete");
     }
     return SBF_OK;
 }

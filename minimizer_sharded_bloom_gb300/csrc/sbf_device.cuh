@@ -14,6 +14,7 @@ namespace sbf {
 constexpr uint64_t kC1 = 0x9E3779B97F4A7C15ull;  // floor(2^64 / golden ratio)
 constexpr uint64_t kC2 = 0x6A09E667F3BCC909ull;  // floor((sqrt(2) - 1) * 2^64) | 1
 constexpr int kStatusBadOffsets = 1;
+constexpr int kStatusTimeout = 2;  // a bounded device wait gave up
 
 // Everything a kernel launch needs; passed by value (kernel parameter space).
 struct LaunchArgs {

@@ -3,7 +3,7 @@
 
 #include <cstdint>
 
-#include "../../include/sbf.h"
+#include "sbf.h"
 
 struct sbf_filter {
     int device = 0;

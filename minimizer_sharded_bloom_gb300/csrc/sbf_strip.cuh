@@ -47,14 +47,21 @@
 
 namespace sbf {
 
-__device__ __forceinline__ uint32_t shl_clamp(uint32_t a, uint32_t s) {
-    uint32_t d;  // PTX shl: shift amounts above 32 give 0
-    asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(s));
-    return d;
-}
-
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+// Flush one run: a 64-bit OR reduction per non-zero word of the shard.  The
+// word values are first copied into registers of their own, so that the
+// accumulator can be reset at once instead of waiting until the reductions
+// have read their operands.
+template <int H>
+__device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
+    uint64_t v[4];
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd)
+        asm volatile("mov.b64 %0, {%1, %2};" : "=l"(v[wd]) : "r"(acc[2 * wd]), "r"(acc[2 * wd + 1]));
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        if (wd >= H) continue;
+        asm volatile("red.global.or.b64 [%0], %1;" ::"l"(F + wd), "l"(v[wd]) : "memory");
+    }
 }
 
 // One 256-bit shard through the non-coherent path (Sec. IV-G).
@@ -119,14 +126,82 @@ __device__ __forceinline__ uint64_t bits64_at(const uint32_t *bm, int bit) {
     return ((uint64_t)hi << 32) | lo;
 }
 
-// 32 bases (64 bits, first base in bit 63..62) starting at code index ci.
-__device__ __forceinline__ uint64_t codes32_at(const uint32_t *codes, int ci) {
+// 64 bases starting at code index ci, as four words w[0..3] (first base in
+// bits 31..30 of w[0]).
+__device__ __forceinline__ void codes64_at(const uint32_t *codes, int ci, uint32_t w[4]) {
     const int wi = ci >> 4, sh = (ci & 15) * 2;
-    const uint32_t a = codes[wi], b = codes[wi + 1], c = codes[wi + 2];
-    const uint32_t hi = __funnelshift_l(b, a, sh);
-    const uint32_t lo = __funnelshift_l(c, b, sh);
-    return ((uint64_t)hi << 32) | lo;
+    uint32_t a[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) a[j] = codes[wi + j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = __funnelshift_l(a[j + 1], a[j], sh);
 }
+
+// The packed value of bases [b, b+t) of a 64-base window (first base most
+// significant): bits [128 - 2(b+t), 128 - 2b) of w[0]:w[1]:w[2]:w[3].  Called
+// with b, t that are constants after unrolling, so every index folds.
+__device__ __forceinline__ uint32_t wsel(const uint32_t w[4], int i) {
+    return (i >= 0 && i < 4) ? w[i] : 0u;
+}
+
+__device__ __forceinline__ uint64_t win_value(const uint32_t w[4], int b, int t) {
+    const int lo = 128 - 2 * (b + t), nbits = 2 * t;
+    const int q = lo >> 5, r = lo & 31;
+    const uint32_t lo32 = r ? __funnelshift_r(wsel(w, 3 - q), wsel(w, 2 - q), r) : wsel(w, 3 - q);
+    if (nbits <= 32) return nbits == 32 ? (uint64_t)lo32 : (uint64_t)(lo32 & ((1u << nbits) - 1u));
+    uint32_t hi32 = r ? __funnelshift_r(wsel(w, 2 - q), wsel(w, 1 - q), r) : wsel(w, 2 - q);
+    if (nbits < 64) hi32 &= (1u << (nbits - 32)) - 1u;
+    return ((uint64_t)hi32 << 32) | lo32;
+}
+
+// x * b for b in {0, 1}: keeps or clears x with one integer multiply-add
+// (issued on the FMA pipe, which the logic-heavy loop leaves idle).
+__device__ __forceinline__ uint32_t keep_if(uint32_t x, uint32_t b) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, 0;" : "=r"(d) : "r"(x), "r"(b));
+    return d;
+}
+
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- TMA bulk copy (global -> shared) completed on an mbarrier.
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Bounded wait: false after ~2^22 polls (the copy never completed).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (int it = 0; it < (1 << 22); ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// 16-byte asynchronous global -> shared copy through L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int K_, int M_, int S_, int H_>
 struct StripCfg {
@@ -141,8 +216,8 @@ struct StripCfg {
     static constexpr int CODE_WORDS = (TILE + K + 96) / 16 + 4;  // 16 bases per word
     static constexpr int BIT_WORDS = (CODE_WORDS + 1) / 2 + 2;   // one bit per code index
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
-    static constexpr uint64_t MASK_M = (M >= 32) ? ~0ull : ((1ull << (2 * M)) - 1);
-    static constexpr uint64_t MASK_S = (S >= 32) ? ~0ull : ((1ull << (2 * S)) - 1);
+    static constexpr int SLOTS = 6;                     // query: staged shards per thread per block
+    static constexpr int RAW_BYTES = 16 * CODE_WORDS;   // a tile's bytes, staged by one bulk copy
     static_assert(W >= 1 && W <= 32 && Z >= 0 && H >= 1 && H <= 10, "parameters");
     static_assert(TILE % 32 == 0, "tile must cover whole output words");
 };
@@ -155,8 +230,11 @@ struct StripSmem {
     uint32_t starts[C::BIT_WORDS];      // record-start bit per code index
     uint32_t valid[C::TILE_WORDS + 2];  // validity bit per k-mer of the tile
     uint32_t outw[C::TILE_WORDS + 2];   // query answer bits of the tile
-    int64_t rec_first;
+    uint64_t raw_bar;                                   // completes the raw bulk copy
+    int abort_flag;
+    alignas(16) unsigned char raw[C::RAW_BYTES];        // the tile's sequence bytes (bulk copy)
 };
+
 
 // The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1).
 template <int H>
@@ -166,17 +244,61 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8]) {
     for (int j = 0; j < 8; ++j) m[j] = 0u;
 #pragma unroll
     for (int i = 0; i < H; ++i) {
-        const uint32_t pos = (uint32_t)(hs >> (i * SW)) & 63u;
-        m[2 * (i & 3)] |= shl_clamp(1u, pos);
-        m[2 * (i & 3) + 1] |= shl_clamp(1u, pos - 32u);
+        const uint64_t one = 1ull << ((uint32_t)(hs >> (i * SW)) & 63u);
+        m[2 * (i & 3)] |= (uint32_t)one;
+        m[2 * (i & 3) + 1] |= (uint32_t)(one >> 32);
     }
+}
+
+// First record boundary r in [0, n] with offsets[r] > x (n + 1 if none), by
+// one warp: an interpolation probe of 32 consecutive boundaries around the
+// guess for evenly sized records, then 32-way searches (one load round each).
+__device__ __forceinline__ int64_t warp_find_boundary(const int64_t *off, int64_t n, int64_t x, int64_t lo,
+                                                      int64_t hi, int lane) {
+    int64_t r_lo = 0, r_hi = n + 1;  // offsets[r] <= x for r < r_lo; > x for r >= r_hi
+    {
+        const double frac = hi > lo ? (double)(x - lo) / (double)(hi - lo) : 0.0;
+        int64_t g = (int64_t)(frac * (double)n);
+        g = g < 0 ? 0 : (g > n ? n : g);
+        int64_t p = g - 15 + lane;
+        p = p < 0 ? 0 : (p > n ? n : p);
+        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
+        const int64_t p31 = __shfl_sync(0xffffffffu, p, 31);
+        if (b == 0) {
+            r_lo = p31 + 1;
+        } else {
+            const int f = __ffs(b) - 1;
+            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
+            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
+            r_hi = pf;
+            if (f > 0) r_lo = pf1 + 1;
+        }
+    }
+    while (r_lo < r_hi) {
+        const int64_t span = r_hi - r_lo;
+        const int64_t p = r_lo + (span * lane) / 32;
+        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
+        if (b == 0) {
+            r_lo = __shfl_sync(0xffffffffu, p, 31) + 1;
+        } else {
+            const int f = __ffs(b) - 1;
+            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
+            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
+            r_hi = pf;
+            if (f > 0) r_lo = pf1 + 1;
+        }
+    }
+    return r_lo;
 }
 
 template <int K, int M, int S, int H, bool kQuery>
 __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchArgs a) {
     using C = StripCfg<K, M, S, H>;
     constexpr int W = C::W, Z = C::Z, NB = C::NB, L = C::L, NT = C::NT, TILE = C::TILE;
+    constexpr int R = C::SLOTS;
     __shared__ StripSmem<K, M, S, H> sm;
+    // query: shards of the current block's run heads, [slot][half][thread]
+    __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
 
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
     const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
@@ -189,60 +311,101 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
     const uint64_t seed_m = a.seed, seed_s = ~a.seed;
     const uint32_t *bad32 = reinterpret_cast<const uint32_t *>(sm.bad16);
 
+    // The bytes of a tile whose 16-aligned span lies inside [lo, hi) arrive by
+    // one bulk copy (TMA) issued while the previous tile computes; other tiles
+    // (the batch's edges, or an unaligned seq) load their bytes directly.
+    auto bulk_ok = [&](int64_t tl) {
+        const int64_t a0 = base + tl * TILE - 16;
+        return aligned && a0 >= lo && a0 + C::RAW_BYTES <= hi;
+    };
+    if (tid == 0) {
+        mbar_init(&sm.raw_bar, 1);
+        sm.abort_flag = 0;
+    }
+    __syncthreads();
+    uint32_t raw_phase = 0;
+    if (tid == 0 && blockIdx.x < n_tiles && bulk_ok(blockIdx.x))
+        bulk_load(sm.raw, a.seq + (base + (int64_t)blockIdx.x * TILE - 16), C::RAW_BYTES, &sm.raw_bar);
+
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         const int64_t T0 = base + tile * TILE;
         const int64_t A0 = T0 - 16;  // absolute position of code index 0
-        // ---- phase 1: bases -> codes + invalid bits; clear per-tile bitmaps
-        for (int w = tid; w < C::BIT_WORDS; w += NT) sm.starts[w] = 0u;
-        if (kQuery)
-            for (int w = tid; w < C::TILE_WORDS + 2; w += NT) sm.outw[w] = 0u;
-        if (tid < 2) sm.valid[C::TILE_WORDS + tid] = 0u;
-        for (int c = tid; c < C::CODE_WORDS; c += NT) {
-            const int64_t p0 = A0 + 16 * (int64_t)c;
-            uint32_t w[4];
-            if (aligned && p0 >= lo && p0 + 16 <= hi) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.seq + p0));
-                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-            } else {
+        const bool staged = bulk_ok(tile);
+        // ---- phase 1 (warps 1..): bases -> codes + invalid bits.
+        //      phase 1 (warp 0): record starts inside (T0, T0 + TILE + K - 1),
+        //      from a search of the offsets, overlapping the others' encoding.
+        if (tid < 32) {
+            for (int w = tid; w < C::BIT_WORDS; w += 32) sm.starts[w] = 0u;
+            if (tid < 2) sm.valid[C::TILE_WORDS + tid] = 0u;
+            const int64_t r0 = warp_find_boundary(a.offsets, a.n, T0, lo, hi, tid);
+            __syncwarp();
+            const int64_t lim = T0 + TILE + K - 1;
+            bool more = true;
+            for (int64_t rb = r0; more; rb += 4 * 32) {
+                int64_t p[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t x = 0;
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t r = rb + tid + 32 * j;
+                    p[j] = r <= a.n ? a.offsets[r] : lim;
+                }
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const int64_t p = p0 + 4 * q + b;
-                        const uint32_t byte = (p >= lo && p < hi) ? (uint32_t)a.seq[p] : 0u;
-                        x |= byte << (8 * b);
+                for (int j = 0; j < 4; ++j) {
+                    if (p[j] < lim) {
+                        const int ci = (int)(p[j] - A0);
+                        atomicOr(&sm.starts[ci >> 5], 1u << (ci & 31));
                     }
-                    w[q] = x;
+                }
+                more = __any_sync(0xffffffffu, p[3] < lim);
+            }
+        } else {
+            if (kQuery)
+                for (int w = tid - 32; w < C::TILE_WORDS + 2; w += NT - 32) sm.outw[w] = 0u;
+            if (staged) {
+                if (!mbar_wait(&sm.raw_bar, raw_phase)) sm.abort_flag = 1;
+                for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sm.raw + 16 * c);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t code, bad;
+                    encode16(w, code, bad);
+                    sm.codes[c] = code;
+                    sm.bad16[c] = (uint16_t)bad;
+                }
+            } else {
+                for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
+                    const int64_t p0 = A0 + 16 * (int64_t)c;
+                    uint32_t w[4];
+                    if (aligned && p0 >= lo && p0 + 16 <= hi) {
+                        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.seq + p0));
+                        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t x = 0;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                const int64_t pp = p0 + 4 * q + b;
+                                const uint32_t byte = (pp >= lo && pp < hi) ? (uint32_t)a.seq[pp] : 0u;
+                                x |= byte << (8 * b);
+                            }
+                            w[q] = x;
+                        }
+                    }
+                    uint32_t code, bad;
+                    encode16(w, code, bad);
+                    sm.codes[c] = code;
+                    sm.bad16[c] = (uint16_t)bad;
                 }
             }
-            uint32_t code, bad;
-            encode16(w, code, bad);
-            sm.codes[c] = code;
-            sm.bad16[c] = (uint16_t)bad;
+            for (int c = C::CODE_WORDS + tid - 32; c < 2 * C::BIT_WORDS; c += NT - 32) sm.bad16[c] = 0xFFFFu;
         }
-        for (int c = C::CODE_WORDS + tid; c < 2 * C::BIT_WORDS; c += NT) sm.bad16[c] = 0xFFFFu;
-        if (tid == 0) {
-            // first record boundary r (0..n) with offsets[r] > T0
-            int64_t r_lo = 0, r_hi = a.n + 1;
-            while (r_lo < r_hi) {
-                const int64_t mid = r_lo + ((r_hi - r_lo) >> 1);
-                if (a.offsets[mid] > T0) r_hi = mid; else r_lo = mid + 1;
-            }
-            sm.rec_first = r_lo;
+        if (staged) raw_phase ^= 1u;
+        if (__syncthreads_or(sm.abort_flag)) {
+            if (tid == 0) atomicOr(a.status, kStatusTimeout);
+            return;
         }
-        __syncthreads();
-        // ---- phase 2: record starts inside (T0, T0 + TILE + K - 1)
-        {
-            const int64_t lim = T0 + TILE + K - 1;
-            for (int64_t r = sm.rec_first + tid; r <= a.n; r += NT) {
-                const int64_t p = a.offsets[r];
-                if (p >= lim) break;
-                const int ci = (int)(p - A0);
-                atomicOr(&sm.starts[ci >> 5], 1u << (ci & 31));
-            }
-        }
-        __syncthreads();
+        // the raw buffer is free again: start the next tile's copy
+        if (tid == 0 && tile + gridDim.x < n_tiles && bulk_ok(tile + gridDim.x))
+            bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * TILE - 16), C::RAW_BYTES, &sm.raw_bar);
         // ---- phase 3: validity bit per k-mer: no invalid base in its k bases,
         // no record start among its bases 1 .. k-1.
         for (int v = tid; v < C::TILE_WORDS; v += NT) {
@@ -255,43 +418,31 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
         // ---- phase 4: strips
         const int kk0 = tid * L;  // first k-mer of this thread (tile relative)
         if (T0 + kk0 < hi) {
-            // m-front: m-mer u of the strip starts at code index kk0 + 15 + u
-            // (the strip's first k-mer is u = 1); s-front follows the k-mers.
-            uint64_t rm = 0, rs = 0;
+            // m-mer u of the strip starts at code index kk0 + 15 + u; the strip's
+            // k-mers are u = 1 .. L (k-mer kk0 + u - 1 starts at code index kk0 + 16 + u - 1).
             uint64_t suf[W];
             uint32_t shard[W];
             uint32_t mk[Z + 1][8];
 #pragma unroll
-            for (int i = 0; i < W; ++i) suf[i] = ~0ull;
-#pragma unroll
-            for (int z = 0; z <= Z; ++z)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) mk[z][j] = 0u;
-            // warm-up of the m-front: bases u = 0 .. M-2
-            {
-                const uint64_t win = codes32_at(sm.codes, kk0 + 15);
-#pragma unroll
-                for (int b = 0; b < M - 1; ++b) rm = (rm << 2) | ((win >> (62 - 2 * b)) & 3u);
+            for (int i = 0; i < W; ++i) {
+                suf[i] = ~0ull;
+                shard[i] = 0u;
             }
-            // warm-up of the s-front: bases of k-mer kk0 except its last one,
-            // computing the first Z s-mers.
+            // the first Z s-mers of the strip's first k-mer
             {
-                const uint64_t win = codes32_at(sm.codes, kk0 + 16);
+                uint32_t wv[4];
+                codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
-                for (int b = 0; b < K - 1; ++b) {
-                    rs = (rs << 2) | ((win >> (62 - 2 * b)) & 3u);
-                    if (b >= S - 1) {
+                for (int z = 0; z < Z; ++z)
+                    smer_halves<H>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1]);
 #pragma unroll
-                        for (int z = 0; z < Z; ++z)
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) mk[z][j] = mk[z + 1][j];
-                        smer_halves<H>(hash_smer(rs & C::MASK_S, seed_s), mk[Z]);
-                    }
-                }
+                for (int j = 0; j < 8; ++j) mk[0][j] = 0u;
             }
-            // run / answer state
-            uint32_t cur = 0;
-            bool cur_v = false;
+            // run / answer state.  Insert keys a k-mer's run by its shard with bit
+            // 31 set when the k-mer is invalid (shards are < 2^31 here), so an
+            // invalid k-mer never matches a valid run and a run is flushed only
+            // if its key is valid.
+            uint32_t cur_key = 0x80000000u;
             uint32_t acc[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = 0u;
@@ -300,85 +451,116 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
 
 #pragma unroll 1
             for (int blk = 0; blk <= NB; ++blk) {
-                // -- pass A: m-mers u = blk*W .. blk*W + W-1; emits the shards of
+                // -- pass A: m-mers u = blk*W .. blk*W + W-1; emits the keys of
                 //    k-mers u = (blk-1)*W + 1 .. blk*W (the strip's block blk-1).
+                //    Query: every run head's shard is copied to a slot (cp.async)
+                //    and flagged in `heads`.
+                int nh = 0;
+                uint32_t heads = 0;
+                const uint32_t last_before = shard[W - 1];
+                const int kb = kk0 + (blk - 1) * W;
+                uint64_t vwin = 0;
+                if (blk > 0) vwin = bits64_at(sm.valid, kb);
                 {
-                    const uint64_t win = codes32_at(sm.codes, kk0 + 15 + blk * W + M - 1);
+                    uint32_t wv[4];
+                    codes64_at(sm.codes, kk0 + 15 + blk * W, wv);
                     uint64_t h[W];
                     uint64_t pre = ~0ull;
 #pragma unroll
                     for (int i = 0; i < W; ++i) {
-                        rm = (rm << 2) | ((win >> (62 - 2 * i)) & 3u);
-                        h[i] = hash_minimizer(rm & C::MASK_M, seed_m);
+                        h[i] = hash_minimizer(win_value(wv, i, M), seed_m);
                         pre = h[i] < pre ? h[i] : pre;
                         if (i < W - 1) {
                             const uint64_t mu = suf[i + 1] < pre ? suf[i + 1] : pre;
                             shard[i] = (uint32_t)mu & smask;
+                            if (kQuery && blk > 0) {
+                                const bool head = (i == 0) ? (blk == 1 || shard[0] != last_before)
+                                                           : (shard[i] != shard[i - 1]);
+                                if (head) {
+                                    heads |= 1u << i;
+                                    if (nh < R) {
+                                        const uint64_t *src = words + (uint64_t)shard[i] * 4;
+                                        cp_async16(smem_u32(&slot_mem[(nh * 2 + 0) * NT + tid]), src);
+                                        cp_async16(smem_u32(&slot_mem[(nh * 2 + 1) * NT + tid]), src + 2);
+                                    }
+                                    ++nh;
+                                }
+                            }
                         }
                     }
+                    if (kQuery) cp_async_commit();
                     suf[W - 1] = h[W - 1];
 #pragma unroll
                     for (int i = W - 2; i >= 0; --i) suf[i] = h[i] < suf[i + 1] ? h[i] : suf[i + 1];
                     shard[W - 1] = (uint32_t)suf[0] & smask;
                     if (kQuery && blk > 0) {
-#pragma unroll
-                        for (int i = 0; i < W; ++i)
-                            if (i == 0 || shard[i] != shard[i - 1]) prefetch_l1(words + (uint64_t)shard[i] * 4);
+                        const bool head = (W == 1) ? (blk == 1 || shard[0] != last_before)
+                                                   : (shard[W - 1] != shard[W > 1 ? W - 2 : 0]);
+                        if (head) {
+                            heads |= 1u << (W - 1);
+                            if (nh < R) {
+                                const uint64_t *src = words + (uint64_t)shard[W - 1] * 4;
+                                cp_async16(smem_u32(&slot_mem[(nh * 2 + 0) * NT + tid]), src);
+                                cp_async16(smem_u32(&slot_mem[(nh * 2 + 1) * NT + tid]), src + 2);
+                            }
+                        }
                     }
+                    if (kQuery) cp_async_commit();
                 }
                 if (blk == 0) continue;
-                // -- pass B: k-mers kk = kk0 + (blk-1)*W + i
+                // -- pass B: k-mers kk = kb + i; the newest s-mer of k-mer kk starts at
+                //    code index kk + 16 + Z.
                 {
-                    const int kb = kk0 + (blk - 1) * W;
-                    const uint64_t win = codes32_at(sm.codes, kb + 16 + K - 1);
-                    const uint64_t vwin = bits64_at(sm.valid, kb);
+                    uint32_t wv[4];
+                    codes64_at(sm.codes, kb + 16 + Z, wv);
                     uint32_t present = 0;
+                    int nb = 0;
+                    if (kQuery) cp_async_wait<1>();
 #pragma unroll
                     for (int i = 0; i < W; ++i) {
-                        rs = (rs << 2) | ((win >> (62 - 2 * i)) & 3u);
 #pragma unroll
                         for (int z = 0; z < Z; ++z)
 #pragma unroll
                             for (int j = 0; j < 8; ++j) mk[z][j] = mk[z + 1][j];
-                        smer_halves<H>(hash_smer(rs & C::MASK_S, seed_s), mk[Z]);
-                        uint32_t km[8];
+                        smer_halves<H>(hash_smer(win_value(wv, i, S), seed_s), mk[Z]);
+                        // OR of the k-mer's older s-mers (its newest is mk[Z])
+                        uint32_t older[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            uint32_t x = mk[0][j];
+                            uint32_t x = 0u;
 #pragma unroll
-                            for (int z = 1; z <= Z; ++z) x |= mk[z][j];
-                            km[j] = x;
+                            for (int z = 0; z < Z; ++z) x |= mk[z][j];
+                            older[j] = x;
                         }
-                        const bool v = (vwin >> i) & 1u;
-                        const uint32_t sh = shard[i];
                         if (!kQuery) {
-                            const bool same = v && cur_v && sh == cur;
-                            if (cur_v && !same) {
-                                uint64_t *F = words + (uint64_t)cur * 4;
+                            const uint32_t key = shard[i] | ((((uint32_t)(vwin >> i)) & 1u) ^ 1u) << 31;
+                            if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                            const uint32_t same = key == cur_key ? 1u : 0u;
 #pragma unroll
-                                for (int wd = 0; wd < 4; ++wd) {
-                                    if (wd >= H) continue;
-                                    const uint64_t val = ((uint64_t)acc[2 * wd + 1] << 32) | acc[2 * wd];
-                                    atomicOr(reinterpret_cast<unsigned long long *>(F + wd), val);
-                                }
-                            }
-                            const uint32_t keep = same ? ~0u : 0u;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[j] = (acc[j] & keep) | km[j];
-                            cur = sh;
-                            cur_v = v;
+                            for (int j = 0; j < 8; ++j) acc[j] = keep_if(acc[j], same) | older[j] | mk[Z][j];
+                            cur_key = key;
                         } else {
-                            if (v && (!cur_v || sh != cur)) {
-                                load_shard(words + (uint64_t)sh * 4, F0, F1, F2, F3);
-                                cur = sh;
-                                cur_v = true;
+                            if (i == W - 1) cp_async_wait<0>();
+                            if ((heads >> i) & 1u) {
+                                if (nb < R) {
+                                    const uint4 lo4 = slot_mem[(nb * 2 + 0) * NT + tid];
+                                    const uint4 hi4 = slot_mem[(nb * 2 + 1) * NT + tid];
+                                    F0 = ((uint64_t)lo4.y << 32) | lo4.x;
+                                    F1 = ((uint64_t)lo4.w << 32) | lo4.z;
+                                    F2 = ((uint64_t)hi4.y << 32) | hi4.x;
+                                    F3 = ((uint64_t)hi4.w << 32) | hi4.z;
+                                } else {
+                                    load_shard(words + (uint64_t)shard[i] * 4, F0, F1, F2, F3);
+                                }
+                                ++nb;
                             }
-                            const uint32_t miss =
-                                (km[0] & ~(uint32_t)F0) | (km[1] & ~(uint32_t)(F0 >> 32)) |
-                                (km[2] & ~(uint32_t)F1) | (km[3] & ~(uint32_t)(F1 >> 32)) |
-                                (km[4] & ~(uint32_t)F2) | (km[5] & ~(uint32_t)(F2 >> 32)) |
-                                (km[6] & ~(uint32_t)F3) | (km[7] & ~(uint32_t)(F3 >> 32));
-                            present |= (uint32_t)(v && miss == 0u) << i;
+                            const uint32_t f[8] = {(uint32_t)F0, (uint32_t)(F0 >> 32), (uint32_t)F1,
+                                                   (uint32_t)(F1 >> 32), (uint32_t)F2, (uint32_t)(F2 >> 32),
+                                                   (uint32_t)F3, (uint32_t)(F3 >> 32)};
+                            uint32_t miss = 0u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) miss |= (older[j] | mk[Z][j]) & ~f[j];
+                            present |= (uint32_t)(((vwin >> i) & 1u) && miss == 0u) << i;
                         }
                     }
                     if (kQuery && present) {
@@ -388,15 +570,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                     }
                 }
             }
-            if (!kQuery && cur_v) {
-                uint64_t *F = words + (uint64_t)cur * 4;
-#pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-                    if (wd >= H) continue;
-                    const uint64_t val = ((uint64_t)acc[2 * wd + 1] << 32) | acc[2 * wd];
-                    atomicOr(reinterpret_cast<unsigned long long *>(F + wd), val);
-                }
-            }
+            if (!kQuery && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
         }
         __syncthreads();
         if (kQuery) {
