@@ -100,15 +100,21 @@ int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int6
               uint32_t *out_bits, void *stream);
 
 /* Host-facing insert: seq and offsets are HOST pointers (pageable or
- * pinned), same layout as sbf_insert.  The records are staged to the device in
- * chunks through pinned buffers on two alternating streams, overlapping copies
- * with kernels (Sec. IV-G, host FASTX staging).  Returns when the filter holds
- * every k-mer.  `stream` (may be NULL) is made to wait for the work. */
+ * pinned), same layout as sbf_insert.  Returns when the filter holds every
+ * k-mer; the work is ordered after earlier work on `stream` (may be NULL).
+ * When the device can access the buffers in place -- page-locked memory, or
+ * pageable memory on a device with pageable-memory access through the host
+ * page tables (Grace systems over NVLink-C2C) -- the kernels read them
+ * directly, with no copies.  Otherwise (or after sbf_set_host_mode(f, 1)) the
+ * records are staged to the device in chunks through pinned buffers on two
+ * alternating streams, overlapping copies with kernels (Sec. IV-G, host FASTX
+ * staging). */
 int sbf_insert_host(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                     void *stream);
 
 /* Host-facing query: seq/offsets/out_bits are HOST pointers, same layout and
- * output contract as sbf_query.  Returns when out_bits is complete. */
+ * output contract as sbf_query.  Returns when out_bits is complete.  Reads and
+ * writes the host buffers in place or stages them, as sbf_insert_host. */
 int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                    uint32_t *out_bits, void *stream);
 
@@ -131,7 +137,11 @@ int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets,
 int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                            uint32_t *out_bits, void *stream);
 
-/* Chunk size of the host-facing calls, in sequence positions (default 2^27;
+/* Host-facing access mode: 0 (default) reads host buffers in place when the
+ * device can, else stages them; 1 always stages. */
+int sbf_set_host_mode(sbf_filter *f, int mode);
+
+/* Chunk size of the staged host-facing calls, in sequence positions (default 2^27;
  * rounded down to a multiple of 32; at least 32).  Smaller chunks overlap
  * copies and kernels at a finer grain and need smaller staging buffers. */
 int sbf_set_host_chunk(sbf_filter *f, int64_t positions);

@@ -29,6 +29,7 @@ SIGNATURES = {
     "sbf_query_host": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "sbf_query_host_noalloc": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "sbf_set_host_chunk": (_i32, [_vp, _i64]),
+    "sbf_set_host_mode": (_i32, [_vp, _i32]),
     "sbf_copy_bits": (_i32, [_vp, _vp, _u64, _vp]),
     "sbf_load_bits": (_i32, [_vp, _vp, _u64, _vp]),
     "sbf_clear": (_i32, [_vp, _vp]),
@@ -118,6 +119,10 @@ def sbf_query_host_noalloc(f: int, seq: int, offsets: int, n: int, out_bits: int
 
 def sbf_set_host_chunk(f: int, positions: int) -> None:
     check(load().sbf_set_host_chunk(f, positions), "sbf_set_host_chunk")
+
+
+def sbf_set_host_mode(f: int, mode: int) -> None:
+    check(load().sbf_set_host_mode(f, mode), "sbf_set_host_mode")
 
 
 def sbf_copy_bits(f: int, dst: int, dst_bytes: int, stream: int = 0) -> None:

@@ -100,7 +100,7 @@ int launch_check(const sbf_filter *f, const int64_t *offsets, int64_t n, cudaStr
 }
 
 sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
-                          uint32_t *out) {
+                          uint32_t *out, bool device_seq = true) {
     sbf::LaunchArgs la;
     la.seq = reinterpret_cast<const uint8_t *>(seq);
     la.offsets = offsets;
@@ -114,6 +114,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.m = f->m;
     la.s = f->s;
     la.H = f->H;
+    la.device_seq = device_seq ? 1 : 0;
     return la;
 }
 
@@ -141,6 +142,24 @@ int sbf::set_error(int code, const char *fmt, ...) {
     vfail(code, fmt, ap);
     va_end(ap);
     return code;
+}
+
+int sbf::launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream,
+                       bool device_seq) {
+    if (n == 0) return SBF_OK;
+    cudaStream_t st = as_stream(stream);
+    if (int rc = launch_check(f, offsets, n, st)) return rc;
+    return launch(f->insert_kernel, f->grid_insert, f->threads,
+                  make_args(f, seq, offsets, n, nullptr, device_seq), st);
+}
+
+int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                      uint32_t *out_bits, void *stream, bool device_seq) {
+    if (n == 0) return SBF_OK;
+    cudaStream_t st = as_stream(stream);
+    if (int rc = launch_check(f, offsets, n, st)) return rc;
+    return launch(f->query_kernel, f->grid_query, f->threads,
+                  make_args(f, seq, offsets, n, out_bits, device_seq), st);
 }
 
 extern "C" {
@@ -250,9 +269,7 @@ int sbf_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n
     if (!f || !seq || !offsets || n < 0) return fail(SBF_ERR_INVALID_ARG, "sbf_insert: bad arguments");
     if (n == 0) return SBF_OK;
     if (int rc = check_device(f)) return rc;
-    cudaStream_t st = as_stream(stream);
-    if (int rc = launch_check(f, offsets, n, st)) return rc;
-    return launch(f->insert_kernel, f->grid_insert, f->threads, make_args(f, seq, offsets, n, nullptr), st);
+    return sbf::launch_insert(f, seq, offsets, n, stream, true);
 }
 
 int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
@@ -261,9 +278,7 @@ int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int6
         return fail(SBF_ERR_INVALID_ARG, "sbf_query: bad arguments");
     if (n == 0) return SBF_OK;
     if (int rc = check_device(f)) return rc;
-    cudaStream_t st = as_stream(stream);
-    if (int rc = launch_check(f, offsets, n, st)) return rc;
-    return launch(f->query_kernel, f->grid_query, f->threads, make_args(f, seq, offsets, n, out_bits), st);
+    return sbf::launch_query(f, seq, offsets, n, out_bits, stream, true);
 }
 
 int sbf_copy_bits(const sbf_filter *f, void *dst, uint64_t dst_bytes, void *stream) {

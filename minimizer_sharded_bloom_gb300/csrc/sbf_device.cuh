@@ -27,6 +27,7 @@ struct LaunchArgs {
     uint64_t shard_mask;      // num_shards - 1
     uint64_t seed;            // minimizer seed; the s-mer seed is ~seed
     int k, m, s, H;
+    int device_seq;           // 1: seq is device memory (tile bytes may use TMA bulk copies)
 };
 
 // Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an

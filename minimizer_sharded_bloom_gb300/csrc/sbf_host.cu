@@ -86,6 +86,50 @@ int host_kind(const void *p) {
     return -1;
 }
 
+// Device alias of host pointer p when kernels can read and write it in place:
+// page-locked memory (its mapped address), or pageable memory on a device that
+// accesses host memory through the host page tables (e.g. over NVLink-C2C).
+// Returns nullptr when p must be staged.
+const void *device_alias(const void *p, int dev) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer ? a.devicePointer : p;
+    if (a.type == cudaMemoryTypeUnregistered) {
+        int pageable = 0;
+        if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) == cudaSuccess && pageable)
+            return p;
+    }
+    return nullptr;
+}
+
+// Read (and for query write) the host buffers in place: one launch, no copies.
+// Returns 1 when done this way, 0 when the buffers are not device-accessible.
+int run_in_place(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint32_t *out_bits,
+                 void *user_stream, bool query, int *rc) {
+    const int64_t lo = off[0], hi = off[n];
+    const void *s_al = device_alias(seq + lo, f->device);
+    const void *o_al = device_alias(off, f->device);
+    const void *q_al = query ? device_alias(out_bits + (lo >> 5), f->device) : nullptr;
+    if (!s_al || !o_al || (query && !q_al)) return 0;
+    // the aliases of the buffers' first used elements, re-biased to index with the caller's offsets
+    const char *dseq = reinterpret_cast<const char *>(reinterpret_cast<uintptr_t>(s_al) - (uintptr_t)lo);
+    const int64_t *doff = static_cast<const int64_t *>(o_al);
+    uint32_t *dout = query ? reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(q_al) -
+                                                           (uintptr_t)(lo >> 5) * sizeof(uint32_t))
+                           : nullptr;
+    *rc = query ? sbf::launch_query(f, dseq, doff, n, dout, user_stream, false)
+                : sbf::launch_insert(f, dseq, doff, n, user_stream, false);
+    if (*rc == SBF_OK) {
+        cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(user_stream));
+        if (e != cudaSuccess) *rc = sbf::set_error(SBF_ERR_CUDA, "host call: %s", cudaGetErrorString(e));
+    }
+    if (*rc == SBF_OK) *rc = sbf_get_status(f, user_stream);
+    return 1;
+}
+
 // First record r with offsets[r + 1] > g.
 int64_t record_at(const int64_t *off, int64_t n, int64_t g) {
     int64_t lo = 0, hi = n - 1;
@@ -114,6 +158,10 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != f->device)
         return set_error(SBF_ERR_INVALID_ARG, "the filter's device is not current");
+    if (f->host_mode == 0) {
+        int rc = SBF_OK;
+        if (run_in_place(f, seq, off, n, out_bits, user_stream, query, &rc)) return rc;
+    }
     if (!f->stager) f->stager = new Stager;
     Stager &st = *static_cast<Stager *>(f->stager);
 
@@ -219,6 +267,12 @@ void sbf::destroy_stager(void *p) {
 }
 
 extern "C" {
+
+int sbf_set_host_mode(sbf_filter *f, int mode) {
+    if (!f || mode < 0 || mode > 1) return sbf::set_error(SBF_ERR_INVALID_ARG, "sbf_set_host_mode: mode is 0 or 1");
+    f->host_mode = mode;
+    return SBF_OK;
+}
 
 int sbf_set_host_chunk(sbf_filter *f, int64_t positions) {
     if (!f || positions < 32) return sbf::set_error(SBF_ERR_INVALID_ARG, "sbf_set_host_chunk: need >= 32 positions");

@@ -20,10 +20,17 @@ struct sbf_filter {
     bool specialized = false;
     void *stager = nullptr;     // host-facing staging buffers, created on first use
     int64_t host_chunk = int64_t(1) << 27;  // host-facing chunk, in positions
+    int host_mode = 0;          // 0: read host buffers in place when possible; 1: always stage
 };
 
 namespace sbf {
 // Records the calling thread's error message and returns `code`.
 int set_error(int code, const char *fmt, ...);
 void destroy_stager(void *stager);
+// Launch the check + insert/query kernels; device_seq = false when seq is host
+// memory read in place (the kernel then loads tile bytes without TMA).
+int launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream,
+                  bool device_seq);
+int launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
+                 uint32_t *out_bits, void *stream, bool device_seq);
 }  // namespace sbf

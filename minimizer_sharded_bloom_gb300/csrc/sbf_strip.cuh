@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
     // (the batch's edges, or an unaligned seq) load their bytes directly.
     auto bulk_ok = [&](int64_t tl) {
         const int64_t a0 = base + tl * TILE - 16;
-        return aligned && a0 >= lo && a0 + C::RAW_BYTES <= hi;
+        return a.device_seq && aligned && a0 >= lo && a0 + C::RAW_BYTES <= hi;
     };
     if (tid == 0) {
         mbar_init(&sm.raw_bar, 1);

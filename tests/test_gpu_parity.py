@@ -205,12 +205,14 @@ def test_copy_load_clear(torch):
     assert not s2.to_numpy().any()
 
 
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("pinned", [False, True])
 @pytest.mark.parametrize("params", [MAIN, dict(k=25, m=11, s=20, H=3)])
-def test_host_entry_points(torch, pinned, params):
-    """sbf_insert_host / sbf_query_host, chunked at 4096 positions so that
-    records and k-mers straddle chunk edges, with pageable and pinned host
-    buffers, equal the oracle."""
+def test_host_entry_points(torch, pinned, params, mode):
+    """sbf_insert_host / sbf_query_host, reading the host buffers in place
+    (mode 0, when the device can) or staged in chunks of 4096 positions so that
+    records and k-mers straddle chunk edges (mode 1), with pageable and pinned
+    host buffers, equal the oracle."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(13)
     ins = synth.random_records(rng, 30, 0, 2500, n_prob=0.002)
@@ -219,6 +221,7 @@ def test_host_entry_points(torch, pinned, params):
                          np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]]))
     sbf = _filter(1 << 14, params, 21)
     N.sbf_set_host_chunk(sbf.handle, 4096)
+    N.sbf_set_host_mode(sbf.handle, mode)
     if pinned:
         def pin(a):
             t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
