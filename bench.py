@@ -168,7 +168,14 @@ def runs_estimate(wl, k=K, m=M):
     return kmer_count(wl, k) * 2.0 / (w + 1) + wl.n_records
 
 
-def fpr_of(words: np.ndarray, qry) -> float | None:
+def fpr_count(qry, k=K) -> int:
+    rnd = qry.meta.get("is_random")
+    if rnd is None:
+        return 0
+    return int(np.maximum(np.diff(qry.offsets)[rnd] - k + 1, 0).sum())
+
+
+def fpr_of(words: np.ndarray, qry, k=K) -> float | None:
     rnd = qry.meta.get("is_random")
     if rnd is None or not rnd.any():
         return None
@@ -177,7 +184,7 @@ def fpr_of(words: np.ndarray, qry) -> float | None:
     hits = total = 0
     for c in range(0, starts.size, 1 << 16):
         st, ln = starts[c:c + (1 << 16)], lens[c:c + (1 << 16)]
-        nk = np.maximum(ln - K + 1, 0)
+        nk = np.maximum(ln - k + 1, 0)
         if nk.sum() == 0:
             continue
         pos = np.repeat(st, nk) + (np.arange(nk.sum()) - np.repeat(np.cumsum(nk) - nk, nk))
@@ -247,7 +254,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="measure every configuration and the sweep grid (one JSON line each)")
     args = ap.parse_args()
+    if args.suite:
+        run_suite(args)
+        return
     rank, world, local = dist_info()
 
     if args.impl == "reference":
@@ -424,6 +436,94 @@ def random_rmw_ceiling(torch, gib: int = 8, rows_touched: int = 25_000_000) -> f
     del F, idx, src
     torch.cuda.empty_cache()
     return rate
+
+
+def _timed(torch, fn, warmup=2, reps=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def run_suite(args):
+    """One JSON line per configuration (tiny, genome-like, irregular) and per
+    point of the (s, m, H) sweep at k = 31 and 2^30 bits: insert and query
+    k-mers/s (CUDA events, device-resident inputs) and the false-positive
+    rate.  Parity of every point is covered by the tests."""
+    import torch
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter, build_lib, _native as N
+    build_lib.build()
+    torch.cuda.set_device(0)
+    st = int(torch.cuda.current_stream().cuda_stream)
+
+    def dev(wl):
+        return torch.from_numpy(wl.seq).cuda(), torch.from_numpy(wl.offsets).cuda()
+
+    def measure(name, ins, qry, bits, k=K, m=M, s=S, H=H, fpr_qry=None, extra=None):
+        sbf = SuperBloomFilter(bits, k=k, m=m, s=s, H=H, seed=SEED)
+        di, dio = dev(ins)
+        dq, dqo = dev(qry)
+        out = torch.zeros((qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
+        t_ins = _timed(torch, lambda: N.sbf_insert(sbf.handle, di.data_ptr(), dio.data_ptr(),
+                                                    ins.n_records, st))
+        t_q = _timed(torch, lambda: N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(),
+                                                 qry.n_records, out.data_ptr(), st))
+        words = out.cpu().numpy().view(np.uint32)
+        fq = fpr_qry or qry
+        if fpr_qry is not None:
+            df, dfo = dev(fpr_qry)
+            fout = torch.zeros((fpr_qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
+            N.sbf_query(sbf.handle, df.data_ptr(), dfo.data_ptr(), fpr_qry.n_records, fout.data_ptr(), st)
+            torch.cuda.synchronize()
+            words = fout.cpu().numpy().view(np.uint32)
+            del df, dfo, fout
+        if name == "irregular":
+            # every record is uniform-random and holds N runs: count the valid
+            # k-mers by querying against an all-ones image (each valid k-mer
+            # answers 1), then FPR = positives / valid k-mers
+            lo_w, hi_w = int(qry.offsets[0]) >> 5, (int(qry.offsets[-1]) + 31) >> 5
+            positives = int(np.unpackbits(words[lo_w:hi_w].view(np.uint8)).sum())
+            ones = torch.full((sbf.num_shards, 4), -1, dtype=torch.int64, device="cuda")
+            sbf.load(ones)
+            out.zero_()
+            N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), qry.n_records, out.data_ptr(), st)
+            torch.cuda.synchronize()
+            allw = out.cpu().numpy().view(np.uint32)
+            n_valid = int(np.unpackbits(allw[lo_w:hi_w].view(np.uint8)).sum())
+            fpr, n_fpr = positives / max(n_valid, 1), n_valid
+            del ones
+        else:
+            fpr, n_fpr = fpr_of(words, fq, k), fpr_count(fq, k)
+        line = {"suite": name, "k": k, "m": m, "s": s, "H": H, "filter_bits": bits,
+                "specialized": sbf.specialized, "insert_kmers": kmer_count(ins, k),
+                "query_kmers": kmer_count(qry, k),
+                "insert_kmers_per_s": kmer_count(ins, k) / t_ins,
+                "query_kmers_per_s": kmer_count(qry, k) / t_q, "fpr": fpr,
+                "fpr_kmers": n_fpr}
+        line.update(extra or {})
+        print(json.dumps(line), flush=True)
+        sbf.close()
+
+    ins, qry = synth.tiny()
+    measure("tiny", ins, qry, 1 << 20)
+    g_ins, g_qry = synth.genome_like()
+    measure("genome-like", g_ins, g_qry, 1 << 30)
+    sweep_q = synth.sweep_queries(g_ins)
+    for s_ in (20, 24, 28, 31):
+        for m_ in (12, 14, 16, 18, 21):
+            for H_ in (1, 2, 4, 6, 8):
+                measure("sweep", g_ins, g_qry, 1 << 30, m=m_, s=s_, H=H_, fpr_qry=sweep_q,
+                        extra={"fpr_queries": "10,000,000 uniform 31-mers absent from the inserted set"})
+    del g_ins, g_qry, sweep_q
+    i_ins, i_qry = synth.irregular()
+    i_qry.meta["is_random"] = np.ones(i_qry.n_records, dtype=bool)
+    measure("irregular", i_ins, i_qry, 1 << 32)
 
 
 def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
