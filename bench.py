@@ -157,6 +157,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(pg, values):
+    """Element-wise maximum of a list of floats over all ranks (gloo, CPU
+    tensors); the values themselves on a single rank."""
+    if pg is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def throughput(world: int, steps: int, kmers_per_step: int, seconds: float) -> float:
+    """Whole-job k-mers/s: every rank processes the same per-step work
+    (weak scaling, replicas) within the slowest rank's time."""
+    return world * steps * kmers_per_step / seconds
+
+
 def kmer_count(wl, k=K):
     return wl.kmer_positions(k)
 
@@ -324,18 +341,13 @@ def main():
     t_ins = [ev[i][0].elapsed_time(ev[i][1]) / 1e3 for i in range(args.steps)]
     t_q = [ev[i][1].elapsed_time(ev[i][2]) / 1e3 for i in range(args.steps)]
     total = sum(t_ins) + sum(t_q)
-    if pg:
-        t = torch.tensor([total, sum(t_ins), sum(t_q)], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total, s_ins, s_q = (float(x) for x in t)
-    else:
-        s_ins, s_q = sum(t_ins), sum(t_q)
+    total, s_ins, s_q = max_over_ranks(pg, [total, sum(t_ins), sum(t_q)])
     if sbf.status() != 0:
         raise RuntimeError("device status error in the timed region")
 
     words = out.cpu().numpy().view(np.uint32)
     fpr = fpr_of(words, qry)
-    value = world * args.steps * (nk_ins + nk_q) / total
+    value = throughput(world, args.steps, nk_ins + nk_q, total)
 
     # rooflines: insert against HBM (one 32-byte sector read and written per
     # run), query against the ALU pipe; "roofline" is the dominant (longer) one.
@@ -399,8 +411,8 @@ def main():
                              if args.workload == "out-of-cache" else "see workload",
                        "filter_between_steps": "not cleared (insert is idempotent; same work)",
                        "replicas": world},
-            "insert_kmers_per_s": world * args.steps * nk_ins / s_ins,
-            "query_kmers_per_s": world * args.steps * nk_q / s_q,
+            "insert_kmers_per_s": throughput(world, args.steps, nk_ins, s_ins),
+            "query_kmers_per_s": throughput(world, args.steps, nk_q, s_q),
             "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
             "roofline": roofline, "roofline_other_kernel": roofline_other,
             "gpu_launches": 4 * args.steps,
@@ -520,6 +532,9 @@ def run_suite(args):
             for H_ in (1, 2, 4, 6, 8):
                 measure("sweep", g_ins, g_qry, 1 << 30, m=m_, s=s_, H=H_, fpr_qry=sweep_q,
                         extra={"fpr_queries": "10,000,000 uniform 31-mers absent from the inserted set"})
+    for H_ in (12, 16):  # the paper's larger hash counts (salted multiply, Sec. IV-G)
+        measure("sweep", g_ins, g_qry, 1 << 30, m=16, s=28, H=H_, fpr_qry=sweep_q,
+                extra={"fpr_queries": "10,000,000 uniform 31-mers absent from the inserted set"})
     del g_ins, g_qry, sweep_q
     i_ins, i_qry = synth.irregular()
     i_qry.meta["is_random"] = np.ones(i_qry.n_records, dtype=bool)
@@ -550,13 +565,10 @@ def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
         one()
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
-    if pg:
-        t = torch.tensor([dt], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        dt = float(t[0])
+    dt = max_over_ranks(pg, [dt])[0]
     h2d = ins.seq.nbytes + ins.offsets.nbytes + qry.seq.nbytes + qry.offsets.nbytes
     d2h = 4 * ((qry.n_bases + 31) // 32)
-    return {"value": world * steps * nk_total / dt, "unit": "k-mers/s",
+    return {"value": throughput(world, steps, nk_total, dt), "unit": "k-mers/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": 1e3 * dt / steps,
             "path": "sbf_insert_host + sbf_query_host, pinned host buffers, host wall clock"}

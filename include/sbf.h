@@ -20,8 +20,9 @@
  *     (floor((sqrt2-1)*2^64) | 1); minimizer hash t = (x ^ seed) * C1,
  *     hm = t ^ (t >> 32); s-mer hash t = (x ^ ~seed) * C1, t ^= t >> 32,
  *     t *= C2, t ^= t >> 29 (all mod 2^64); shard = min hm & (num_shards-1);
- *   - hash i of an s-mer sets bit ((hs >> (i * floor(64/H))) & 63) of word
- *     i mod 4;
+ *   - hash i of an s-mer sets, in word i mod 4, bit ((hs >> (i * floor(64/H)))
+ *     & 63) while floor(64/H) >= 6 (H <= 10), else bit (hs * salt(i)) >> 58
+ *     with salt(i) = SplitMix64 output i from state 0, made odd;
  *   - records are CSR slices of one buffer; a k-mer never spans two records;
  *   - forward strand only.
  *
@@ -69,7 +70,7 @@ typedef enum {
  * Shard count = ceil(num_bits / 256) rounded up to a power of two (Sec. IV-B);
  * the device array holds num_shards * 32 bytes.
  * Requires num_bits >= 1, num_shards <= 2^40, 1 <= m <= k <= 32,
- * 1 <= s <= k and 1 <= H <= 10 (bit-slicing needs floor(64/H) >= 6, Sec. IV-G).
+ * 1 <= s <= k and 1 <= H <= 32 (H > 10 uses the salted multiply, Sec. IV-G).
  * seed selects the hash functions (minimizer seed = seed, s-mer seed = ~seed).
  * Returns NULL on error (SBF_ERR_INVALID_ARG / _OOM / _CUDA in sbf_last_error). */
 sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed);

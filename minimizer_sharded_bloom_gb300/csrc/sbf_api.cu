@@ -22,6 +22,8 @@
 namespace sbf {
 extern const StripEntry kStripEntriesMain[];
 extern const int kStripCountMain;
+extern const StripEntry kStripEntriesLargeH[];
+extern const int kStripCountLargeH;
 #ifdef SBF_WITH_SWEEP
 #define SBF_DECLARE_UNIT(M, S)                       \
     extern const StripEntry kStripEntriesM##M##S##_[]; \
@@ -38,6 +40,7 @@ bool find_specialized(int k, int m, int s, int H, const void **insert, const voi
     };
     static const Table tables[] = {
         {kStripEntriesMain, &kStripCountMain},
+        {kStripEntriesLargeH, &kStripCountLargeH},
 #ifdef SBF_WITH_SWEEP
 #define SBF_TABLE_UNIT(M, S) {kStripEntriesM##M##S##_, &kStripCountM##M##S##_},
         SBF_SWEEP_UNITS(SBF_TABLE_UNIT)
@@ -176,8 +179,8 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
         fail(SBF_ERR_INVALID_ARG, "need 1 <= m <= k <= 32 and 1 <= s <= k (k=%d m=%d s=%d)", k, m, s);
         return nullptr;
     }
-    if (H < 1 || H > 10) {
-        fail(SBF_ERR_INVALID_ARG, "H must be in 1..10 (bit-slicing needs floor(64/H) >= 6), got %d", H);
+    if (H < 1 || H > sbf::kMaxH) {
+        fail(SBF_ERR_INVALID_ARG, "H must be in 1..%d, got %d", sbf::kMaxH, H);
         return nullptr;
     }
     const uint64_t need = num_bits / 256 + (num_bits % 256 != 0);

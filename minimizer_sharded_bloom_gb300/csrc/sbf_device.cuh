@@ -56,11 +56,33 @@ __device__ __forceinline__ int base_code(uint32_t c) {
     return ok ? code : -1;
 }
 
+// Salt of hash index i for H > 10 (Sec. IV-G: "per-hash-index golden-ratio-
+// derived salt"): output i of SplitMix64 from state 0, whose state advances by
+// the golden-ratio constant, made odd.
+__host__ __device__ constexpr uint64_t salt_of(int i) {
+    uint64_t z = (uint64_t)(i + 1) * kC1;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z | 1ull;
+}
+constexpr int kMaxH = 32;
+__constant__ const uint64_t kSalt[kMaxH] = {
+    salt_of(0),  salt_of(1),  salt_of(2),  salt_of(3),  salt_of(4),  salt_of(5),  salt_of(6),  salt_of(7),
+    salt_of(8),  salt_of(9),  salt_of(10), salt_of(11), salt_of(12), salt_of(13), salt_of(14), salt_of(15),
+    salt_of(16), salt_of(17), salt_of(18), salt_of(19), salt_of(20), salt_of(21), salt_of(22), salt_of(23),
+    salt_of(24), salt_of(25), salt_of(26), salt_of(27), salt_of(28), salt_of(29), salt_of(30), salt_of(31)};
+
 // OR the H bits of one s-mer hash into four word masks (Sec. IV-B: hash i ->
-// word i mod 4; Sec. IV-G: bit-slicing with slice width floor(64/H)).
+// word i mod 4).  Sec. IV-G: bit-slicing with slice width floor(64/H) while it
+// is at least 6 bits; beyond, the top 6 bits of hs * salt(i).
 __device__ __forceinline__ void smer_bits_runtime(uint64_t hs, int H, uint64_t K[4]) {
     const int W = 64 / H;
-    for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);
+    if (W >= 6) {
+        for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);
+    } else {
+        for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs * kSalt[i]) >> 58);
+    }
 }
 
 __device__ __forceinline__ uint64_t low_mask(int symbols) {

@@ -218,7 +218,7 @@ struct StripCfg {
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
     static constexpr int SLOTS = 6;                     // query: staged shards per thread per block
     static constexpr int RAW_BYTES = 16 * CODE_WORDS;   // a tile's bytes, staged by one bulk copy
-    static_assert(W >= 1 && W <= 32 && Z >= 0 && H >= 1 && H <= 10, "parameters");
+    static_assert(W >= 1 && W <= 32 && Z >= 0 && H >= 1 && H <= kMaxH, "parameters");
     static_assert(TILE % 32 == 0, "tile must cover whole output words");
 };
 
@@ -244,7 +244,10 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8]) {
     for (int j = 0; j < 8; ++j) m[j] = 0u;
 #pragma unroll
     for (int i = 0; i < H; ++i) {
-        const uint64_t one = 1ull << ((uint32_t)(hs >> (i * SW)) & 63u);
+        uint32_t pos;
+        if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
+        else pos = (uint32_t)((hs * salt_of(i)) >> 58);
+        const uint64_t one = 1ull << pos;
         m[2 * (i & 3)] |= (uint32_t)one;
         m[2 * (i & 3) + 1] |= (uint32_t)(one >> 32);
     }

@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.orc_hash_m.restype = u64
             L.orc_hash_s.argtypes = [u64, u64]
             L.orc_hash_s.restype = u64
+            L.orc_salt.argtypes = [i32]
+            L.orc_salt.restype = u64
             L.orc_smer_bits.argtypes = [u64, i32, vp]
             L.orc_smer_bits.restype = None
             L.orc_insert.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, u64, u64, i32]

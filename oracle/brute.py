@@ -42,11 +42,26 @@ def hs(x: int, seed: int) -> int:
     return t
 
 
+def salt(i: int) -> int:
+    """Output i of SplitMix64 started at state 0 (state += C1), made odd."""
+    z = ((i + 1) * C1) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    z ^= z >> 31
+    return z | 1
+
+
 def smer_words(h: int, H: int):
+    """Bit i: the low 6 bits of slice i while slices are >= 6 bits wide,
+    otherwise the top 6 bits of h * salt(i) mod 2^64."""
     words = [0, 0, 0, 0]
     width = 64 // H
     for i in range(H):
-        words[i % 4] |= 1 << ((h >> (i * width)) & 63)
+        if width >= 6:
+            pos = (h >> (i * width)) & 63
+        else:
+            pos = ((h * salt(i)) & MASK64) >> 58
+        words[i % 4] |= 1 << pos
     return words
 
 

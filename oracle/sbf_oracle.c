@@ -37,7 +37,9 @@
  *     t = (x ^ seed) * C1; s-mer hash hs(x): t = (x ^ ~seed) * C1,
  *     t ^= t >> 32, t *= C2, t ^= t >> 29 (all mod 2^64);
  *   - bit position of hash i: slice width W = floor(64/H), position =
- *     (hs >> (i*W)) & 63, in word i mod 4; H <= 10 so that W >= 6;
+ *     (hs >> (i*W)) & 63, in word i mod 4, while W >= 6 (H <= 10); for
+ *     11 <= H <= 32, position = top 6 bits of hs * salt(i) mod 2^64, salt(i)
+ *     = SplitMix64 output i from state 0 (golden-ratio increment), made odd;
  *   - records are given as CSR offsets; a k-mer never spans two records;
  *   - the minimum's tie-break is the leftmost window (it cannot change the
  *     result: hm is a bijection, equal hashes mean equal m-mers).
@@ -97,13 +99,32 @@ uint64_t orc_hash_s(uint64_t x, uint64_t seed_s)
     return t;
 }
 
-/* Sec. IV-B + IV-G: the H bits of one s-mer hash, hash i in word i mod 4 at
- * the low 6 bits of slice i (slice width floor(64/H)). */
+/* Salt of hash index i for the large-H fallback: output i of the SplitMix64
+ * generator started at state 0 (its state advances by the golden-ratio
+ * constant C1), made odd. */
+uint64_t orc_salt(int i)
+{
+    uint64_t z = (uint64_t)(i + 1) * ORC_C1;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    z ^= z >> 31;
+    return z | 1u;
+}
+
+/* Sec. IV-B + IV-G: the H bits of one s-mer hash, hash i in word i mod 4.
+ * Bit-slicing while a slice is at least 6 bits wide (64/H >= 6): the position
+ * is the low 6 bits of slice i (slice width floor(64/H)).  For larger H the
+ * paper multiplies by a per-index golden-ratio-derived salt and keeps the
+ * upper bits: position = top 6 bits of hs * salt(i) mod 2^64. */
 void orc_smer_bits(uint64_t hs, int H, uint64_t words[4])
 {
     int W = 64 / H;
     for (int i = 0; i < H; i++) {
-        int pos = (int)((hs >> (i * W)) & 63u);
+        int pos;
+        if (W >= 6)
+            pos = (int)((hs >> (i * W)) & 63u);
+        else
+            pos = (int)((hs * orc_salt(i)) >> 58);
         words[i % 4] |= (uint64_t)1 << pos;
     }
 }
@@ -219,7 +240,7 @@ static int valid_params(const orc_params *P)
 {
     if (P->k < 1 || P->k > 32 || P->m < 1 || P->m > P->k || P->s < 1 || P->s > P->k)
         return 0;
-    if (P->H < 1 || P->H > 10)
+    if (P->H < 1 || P->H > 32)
         return 0;
     if (P->num_shards == 0 || (P->num_shards & (P->num_shards - 1)))
         return 0;

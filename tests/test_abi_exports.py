@@ -63,7 +63,8 @@ def test_argument_errors_need_no_gpu(lib):
     assert not L.sbf_create(0, 31, 16, 28, 4, 0)
     assert "num_bits" in _native.last_error()
     assert not L.sbf_create(1 << 20, 33, 16, 28, 4, 0)
-    assert not L.sbf_create(1 << 20, 31, 16, 28, 11, 0)
+    assert not L.sbf_create(1 << 20, 31, 16, 28, 33, 0)
+    assert not L.sbf_create(1 << 20, 31, 16, 28, 0, 0)
     assert not L.sbf_create(1 << 20, 31, 32, 28, 4, 0)
     assert L.sbf_insert(None, None, None, 1, None) == _native.SBF_ERR_INVALID_ARG
     assert L.sbf_query(None, None, None, 1, None, None) == _native.SBF_ERR_INVALID_ARG

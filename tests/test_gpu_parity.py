@@ -91,7 +91,7 @@ def test_runtime_parameter_kernel(torch, case):
         k = int(rng.integers(1, 33))
         m = int(rng.integers(1, k + 1))
         s = int(rng.integers(1, k + 1))
-        H = int(rng.integers(1, 11))
+        H = int(rng.integers(1, 11)) if case % 3 else int(rng.integers(11, 33))
         if not (k == 31 and m in (12, 14, 16, 18, 21) and s in (20, 24, 28, 31) and H in (1, 2, 4, 6, 8)):
             break
     params = dict(k=k, m=m, s=s, H=H)
@@ -101,6 +101,19 @@ def test_runtime_parameter_kernel(torch, case):
                          np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]]))
     _roundtrip(torch, ins, qry, params, 1 << int(rng.integers(8, 16)), seed=case * 977,
                pad_front=case % 7, expect_specialized=False)
+
+
+@pytest.mark.parametrize("H", [12, 16])
+def test_large_h_specialisations(torch, H):
+    """H = 12, 16 at (31, 16, 28) run specialised kernels with the salted
+    multiply (Sec. IV-G) and match the oracle."""
+    rng = np.random.default_rng(3000 + H)
+    params = dict(k=31, m=16, s=28, H=H)
+    ins = synth.random_records(rng, 4, 5_000, 30_000, n_prob=0.0005)
+    q = synth.Workload(synth.uniform_bases(rng, 2000 * 31), synth.csr(np.full(2000, 31)))
+    qry = synth.Workload(np.concatenate([ins.seq, q.seq]),
+                         np.concatenate([ins.offsets, ins.offsets[-1] + q.offsets[1:]]))
+    _roundtrip(torch, ins, qry, params, 1 << 15, seed=H, expect_specialized=True)
 
 
 def test_edge_cases(torch):

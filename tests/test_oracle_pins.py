@@ -136,9 +136,10 @@ def test_hash_m_low_bits_depend_on_first_base():
 def test_smer_bits_structure():
     """Sec. IV-B / IV-G: hash i lands in word i mod 4; each hash sets exactly
     one bit of its word, so word w holds at most ceil((H - w) / 4) bits and
-    words >= H are empty for H < 4."""
+    words >= H are empty for H < 4 (slicing for H <= 10, salted multiply
+    beyond)."""
     rng = np.random.default_rng(14)
-    for H in range(1, 11):
+    for H in list(range(1, 17)) + [24, 32]:
         for _ in range(200):
             hs = _u64(rng)
             words = oracle.smer_bits(hs, H)
@@ -159,7 +160,7 @@ def test_brute_force_agrees(case):
     k = int(rng.integers(1, 33))
     m = int(rng.integers(1, k + 1))
     s = int(rng.integers(1, k + 1))
-    H = int(rng.integers(1, 11))
+    H = int(rng.integers(1, 11)) if case % 3 else int(rng.integers(11, 33))
     shards = int(2 ** rng.integers(0, 8))
     seed = _u64(rng)
     wl = synth.random_records(rng, int(rng.integers(1, 12)), 0, 160, n_prob=0.02,
@@ -460,3 +461,53 @@ def test_minimizer_density_two_over_w_plus_one(m):
     valid, runs, _ = oracle.count_runs(seq, off, k, m, 28, 4, 1 << 62, 9)
     mean_len = valid / runs
     assert abs(mean_len - (w + 1) / 2) / ((w + 1) / 2) < 0.03, mean_len
+
+
+# SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom number
+# generators", OOPSLA 2014): published first outputs from state 0.
+SPLITMIX64_FROM_ZERO = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_salts_are_splitmix64_outputs():
+    """The large-H salts are the SplitMix64 sequence (golden-ratio increment)
+    made odd: check against the generator's published first outputs."""
+    L = oracle.lib()
+    for i, v in enumerate(SPLITMIX64_FROM_ZERO):
+        assert int(L.orc_salt(i)) == v | 1
+        assert brute.salt(i) == v | 1
+
+
+def test_large_h_positions_are_salted_multiplies():
+    """Sec. IV-G fallback for 64/H < 6: position i = top 6 bits of
+    hs * salt(i) mod 2^64; recomputed here with Python integers."""
+    rng = np.random.default_rng(15)
+    salts = [int(oracle.lib().orc_salt(i)) for i in range(32)]
+    for H in (11, 12, 16, 32):
+        for _ in range(300):
+            hs = _u64(rng)
+            want = [0, 0, 0, 0]
+            for i in range(H):
+                pos = ((hs * salts[i]) % (1 << 64)) >> 58
+                want[i % 4] |= 1 << pos
+            assert oracle.smer_bits(hs, H) == want
+
+
+@pytest.mark.parametrize("H", [12, 16])
+def test_fpr_large_h_matches_popcount_predictor(H):
+    """With H > 10 hashes per s-mer (c_w = H/4 per word), an alien single-s-mer
+    k-mer is a false positive with probability prod_w f_w^(c_w) given the image
+    (f_w = set fraction of word w): the measured rate must match.  A fallback
+    that reused one position per word would inflate the rate far above it."""
+    rng = np.random.default_rng(60 + H)
+    k = s = 31
+    S, seed = 256, 99
+    seq, off = _random_kmers(rng, 3_000, k)
+    F = oracle.insert(np.zeros((S, 4), np.uint64), seq, off, k, 16, s, H, seed)
+    f = np.unpackbits(F.view(np.uint8)).reshape(S, 4, 64).sum(axis=2) / 64.0
+    pred = np.mean(np.prod(f ** (H // 4), axis=1))
+    qseq, qoff = _random_kmers(rng, 200_000, k)
+    out = oracle.query(F, qseq, qoff, k, 16, s, H, seed, nthreads=4)
+    rate, n = _measured_rate(out, qoff, k)
+    assert pred * n >= 10
+    sigma = math.sqrt(pred * (1 - pred) / n)
+    assert abs(rate - pred) < 5 * sigma + 0.05 * pred, (rate, pred)
