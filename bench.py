@@ -216,9 +216,13 @@ def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int
     workload, all host cores."""
     import oracle
     cores = os.cpu_count() or 1
-    r = int(np.searchsorted(ins.offsets, ins.offsets[0] + budget_bases, side="right")) - 1
+    # the first budget_bases positions of the insert stream (records clipped
+    # there) and the first `reads` query records
+    end = int(ins.offsets[0]) + budget_bases
+    off = np.minimum(ins.offsets, end)
+    r = int(np.searchsorted(off, end, side="left"))
     r = max(1, min(r, ins.n_records))
-    s_ins = synth.Workload(ins.seq[:ins.offsets[r]], ins.offsets[:r + 1])
+    s_ins = synth.Workload(ins.seq[:off[r]], off[:r + 1])
     rq = max(1, min(reads, qry.n_records))
     s_q = synth.Workload(qry.seq[:qry.offsets[rq]], qry.offsets[:rq + 1])
     F = oracle.new_filter(bits)
