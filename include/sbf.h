@@ -147,6 +147,52 @@ int sbf_set_host_mode(sbf_filter *f, int mode);
  * copies and kernels at a finer grain and need smaller staging buffers. */
 int sbf_set_host_chunk(sbf_filter *f, int64_t positions);
 
+/* ---- FASTA / FASTQ input (Sec. IV-A: streamed FASTA/FASTQ with transparent
+ * gzip; Sec. IV-F: sequence-native records).  Host code; no GPU needed to read.
+ * A record's bases are its sequence lines joined without line breaks; every
+ * byte is kept as is (bytes outside ACGTacgt are invalid k-mer symbols).
+ * FASTA records start with '>', FASTQ records with '@' (sequence lines up to
+ * the '+' line, then as many quality characters as bases). */
+typedef struct sbf_fastx sbf_fastx; /* an open reader */
+
+/* Open a plain or gzip-compressed FASTA/FASTQ file (gzip needs a libsbf built
+ * with zlib; see sbf_fastx_has_gzip).  NULL on error (sbf_last_error). */
+sbf_fastx *sbf_fastx_open(const char *path);
+
+/* Next batch of whole records: bases into seq (seq_cap bytes), CSR offsets into
+ * offsets (room for max_records + 1 entries, offsets[0] = 0).  Returns the
+ * number of records (0 at end of input) and *bases_out the bytes used, or a
+ * negative sbf_status.  A record that does not fit is kept for the next call;
+ * if it does not fit an empty buffer the call fails with SBF_ERR_INVALID_ARG
+ * and sbf_fastx_pending_bases() gives the size needed. */
+int64_t sbf_fastx_next(sbf_fastx *r, char *seq, int64_t seq_cap, int64_t *offsets, int64_t max_records,
+                       int64_t *bases_out);
+
+/* Bases of the record kept back by sbf_fastx_next (0 if none). */
+int64_t sbf_fastx_pending_bases(const sbf_fastx *r);
+
+void sbf_fastx_close(sbf_fastx *r); /* NULL-safe */
+
+/* 1 if this build reads gzip input, else 0. */
+int sbf_fastx_has_gzip(void);
+
+/* Insert every record of a FASTA/FASTQ file through sbf_insert_host, in
+ * batches of about batch_bases bases (<= 0: 2^28).  *records / *bases (may be
+ * NULL) receive the totals.  Returns when done. */
+int sbf_insert_fastx(sbf_filter *f, const char *path, int64_t batch_bases, int64_t *records, int64_t *bases);
+
+/* Called once per batch by sbf_query_fastx with the batch's bases, offsets
+ * (n + 1 entries, batch-relative) and answer bits (sbf_query's layout, bit g
+ * for batch position g).  A non-zero return stops the scan. */
+typedef int (*sbf_fastx_sink)(void *user, const char *seq, const int64_t *offsets, int64_t n,
+                              const uint32_t *out_bits);
+
+/* Query every record of a FASTA/FASTQ file through sbf_query_host, in batches
+ * of about batch_bases bases, handing each batch's answers to sink.  Returns
+ * SBF_OK, a negative sbf_status, or sink's non-zero value. */
+int sbf_query_fastx(const sbf_filter *f, const char *path, int64_t batch_bases, sbf_fastx_sink sink,
+                    void *user);
+
 /* Copy the raw image (num_shards * 32 bytes: shard-major, four little-endian
  * uint64 words per shard, bit b of word j = (word >> b) & 1) to dst, host or
  * device memory (cudaMemcpyDefault).  dst_bytes must be >= the image size.

@@ -38,7 +38,19 @@ SIGNATURES = {
     "sbf_is_specialized": (_i32, [_vp]),
     "sbf_get_status": (_i32, [_vp, _vp]),
     "sbf_last_error": (ctypes.c_char_p, []),
+    "sbf_fastx_open": (_vp, [ctypes.c_char_p]),
+    "sbf_fastx_next": (_i64, [_vp, _vp, _i64, _vp, _i64, ctypes.POINTER(ctypes.c_int64)]),
+    "sbf_fastx_pending_bases": (_i64, [_vp]),
+    "sbf_fastx_close": (None, [_vp]),
+    "sbf_fastx_has_gzip": (_i32, []),
+    "sbf_insert_fastx": (_i32, [_vp, ctypes.c_char_p, _i64, ctypes.POINTER(ctypes.c_int64),
+                                ctypes.POINTER(ctypes.c_int64)]),
+    "sbf_query_fastx": (_i32, [_vp, ctypes.c_char_p, _i64, _vp, _vp]),
 }
+
+# sbf_fastx_sink: int (*)(void *user, const char *seq, const int64_t *offsets,
+#                         int64_t n, const uint32_t *out_bits)
+FASTX_SINK = ctypes.CFUNCTYPE(ctypes.c_int, _vp, _vp, _vp, _i64, _vp)
 
 _lock = threading.Lock()
 _lib = None
@@ -159,3 +171,43 @@ def sbf_get_status(f: int, stream: int = 0) -> int:
 
 def sbf_last_error() -> str:
     return last_error()
+
+
+def sbf_fastx_open(path: str) -> int:
+    h = load().sbf_fastx_open(path.encode())
+    if not h:
+        raise SBFError(SBF_ERR_INVALID_ARG, "sbf_fastx_open", last_error())
+    return h
+
+
+def sbf_fastx_next(r: int, seq: int, seq_cap: int, offsets: int, max_records: int):
+    bases = ctypes.c_int64(0)
+    n = int(load().sbf_fastx_next(r, seq, seq_cap, offsets, max_records, ctypes.byref(bases)))
+    if n < 0:
+        raise SBFError(n, "sbf_fastx_next", last_error())
+    return n, bases.value
+
+
+def sbf_fastx_pending_bases(r: int) -> int:
+    return int(load().sbf_fastx_pending_bases(r))
+
+
+def sbf_fastx_close(r: int) -> None:
+    load().sbf_fastx_close(r)
+
+
+def sbf_fastx_has_gzip() -> bool:
+    return bool(load().sbf_fastx_has_gzip())
+
+
+def sbf_insert_fastx(f: int, path: str, batch_bases: int = 0):
+    recs, bases = ctypes.c_int64(0), ctypes.c_int64(0)
+    check(load().sbf_insert_fastx(f, path.encode(), batch_bases, ctypes.byref(recs),
+                                  ctypes.byref(bases)), "sbf_insert_fastx")
+    return recs.value, bases.value
+
+
+def sbf_query_fastx(f: int, path: str, sink, batch_bases: int = 0) -> None:
+    """sink(seq_ptr, offsets_ptr, n, bits_ptr) -> int, called per batch."""
+    cb = FASTX_SINK(lambda user, s, o, n, b: int(sink(s, o, n, b) or 0))
+    check(load().sbf_query_fastx(f, path.encode(), batch_bases, cb, None), "sbf_query_fastx")

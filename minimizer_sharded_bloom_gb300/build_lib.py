@@ -23,6 +23,18 @@ CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-DSBF_WI
           f"-I{INCLUDE}"]
 
 
+def have_zlib() -> bool:
+    """gzip input needs zlib's header and library on the build machine."""
+    return os.path.exists("/usr/include/zlib.h") and any(
+        glob.glob(os.path.join(d, "libz.so*")) for d in
+        ("/usr/lib/x86_64-linux-gnu", "/usr/lib/aarch64-linux-gnu", "/usr/lib64", "/usr/lib", "/lib64"))
+
+
+ZLIB = have_zlib()
+if ZLIB:
+    CFLAGS.append("-DSBF_WITH_ZLIB")
+
+
 def nvcc() -> str:
     path = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(path):
@@ -70,7 +82,7 @@ def build(jobs: int | None = None, verbose: bool = False) -> str:
     if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs] + (["-lz"] if ZLIB else [])
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
