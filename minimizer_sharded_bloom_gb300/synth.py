@@ -1,7 +1,7 @@
-"""Seeded synthetic DNA workloads.
+"""Seeded synthetic DNA and protein workloads.
 
-This module only draws inputs: byte sequences over ACGT (plus N runs) and CSR
-offsets.  It holds none of the filter's arithmetic, so both the CUDA path's
+This module only draws inputs: byte sequences over ACGT (plus N runs) or over
+amino-acid letters, and CSR offsets.  It holds none of the filter's arithmetic, so both the CUDA path's
 tests and the CPU oracle's tests may use it.  Every generator uses numpy's
 PCG64 with an explicit seed and is deterministic.
 
@@ -21,13 +21,21 @@ are not available; these workloads stand in for them:
                    in the inserted sequence (seed 7);
 * irregular     -- 200,000 long reads, log-normal lengths (median 8 kbp,
                    sigma 1.0, clipped to [1, 100,000]), ~0.1 % N in runs of
-                   1-50; two independent sets (seeds 8, 9).
+                   1-50; two independent sets (seeds 8, 9);
+* protein_like  -- 500 M residues uniform over the 20 standard amino-acid
+                   letters in log-normal proteins (median 300, sigma 0.6,
+                   clipped to [30, 5,000]); 10 M fragments of 50 residues,
+                   half from the proteins at 1 % substitution, half uniform
+                   (seeds 10, 11).  No protein database is available; the
+                   cuSBF paper evaluates DNA only.
 """
 from __future__ import annotations
 
 import numpy as np
 
 ACGT = np.frombuffer(b"ACGT", dtype=np.uint8)
+# the 20 standard amino acids, sorted
+AMINO20 = np.frombuffer(b"ACDEFGHIKLMNPQRSTVWY", dtype=np.uint8)
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -37,28 +45,30 @@ def _rng(seed: int) -> np.random.Generator:
 _CHUNK = 1 << 26
 
 
-def uniform_bases(rng: np.random.Generator, n: int) -> np.ndarray:
-    """n i.i.d. uniform bases over ACGT (drawn in chunks of 2^26)."""
+def uniform_bases(rng: np.random.Generator, n: int, symbols: np.ndarray = ACGT) -> np.ndarray:
+    """n i.i.d. uniform symbols, ACGT by default (drawn in chunks of 2^26)."""
     out = np.empty(n, dtype=np.uint8)
     for c in range(0, n, _CHUNK):
         m = min(_CHUNK, n - c)
-        out[c:c + m] = ACGT[rng.integers(0, 4, size=m, dtype=np.uint8)]
+        out[c:c + m] = symbols[rng.integers(0, symbols.size, size=m, dtype=np.uint8)]
     return out
 
 
-def substitute(rng: np.random.Generator, seq: np.ndarray, rate: float) -> np.ndarray:
-    """Each base independently, with probability `rate`, becomes one of the
-    other three bases, chosen uniformly.  Returns a new array (chunks of
-    2^26 bases: a uniform draw per base, then a uniform shift of 1..3 for the
-    hit ones)."""
+def substitute(rng: np.random.Generator, seq: np.ndarray, rate: float,
+               symbols: np.ndarray = ACGT) -> np.ndarray:
+    """Each symbol independently, with probability `rate`, becomes one of the
+    other symbols of the (sorted) alphabet, chosen uniformly.  Returns a new
+    array (chunks of 2^26: a uniform draw per symbol, then a uniform shift of
+    1..len-1 for the hit ones)."""
     out = seq.copy()
+    a = symbols.size
     for c in range(0, seq.size, _CHUNK):
         part = out[c:c + _CHUNK]
         hit = np.flatnonzero(rng.random(part.size) < rate)
         if hit.size:
-            idx = np.searchsorted(ACGT, part[hit])  # ACGT is sorted: A<C<G<T
-            shift = rng.integers(1, 4, size=hit.size)
-            part[hit] = ACGT[(idx + shift) % 4]
+            idx = np.searchsorted(symbols, part[hit])
+            shift = rng.integers(1, a, size=hit.size)
+            part[hit] = symbols[(idx + shift) % a]
     return out
 
 
@@ -135,7 +145,8 @@ def genome_like_reference(seed: int = 3, length: int = 50_000_000,
 
 
 def sample_reads(rng: np.random.Generator, source: np.ndarray, source_offsets: np.ndarray,
-                 n_from_source: int, n_random: int, read_len: int, error: float):
+                 n_from_source: int, n_random: int, read_len: int, error: float,
+                 symbols: np.ndarray = ACGT):
     """Reads of read_len bp: n_from_source taken from the source records
     (record chosen with probability proportional to its number of read
     starts, start uniform within it, forward strand, `error` substitution
@@ -163,9 +174,9 @@ def sample_reads(rng: np.random.Generator, source: np.ndarray, source_offsets: n
         reads[src_slots[c:c + chunk]] = source[idx]
     if n_from_source:
         flat = reads[src_slots].reshape(-1)
-        reads[src_slots] = substitute(rng, flat, error).reshape(-1, read_len)
+        reads[src_slots] = substitute(rng, flat, error, symbols).reshape(-1, read_len)
     if n_random:
-        reads[rnd_slots] = uniform_bases(rng, n_random * read_len).reshape(-1, read_len)
+        reads[rnd_slots] = uniform_bases(rng, n_random * read_len, symbols).reshape(-1, read_len)
     is_random = np.zeros(n, dtype=bool)
     is_random[rnd_slots] = True
     return reads.reshape(-1), csr(np.full(n, read_len)), is_random
@@ -285,6 +296,45 @@ def irregular_set(seed: int, n_reads: int = 200_000, median: float = 8_000.0,
 
 def irregular(seed_insert: int = 8, seed_query: int = 9, **kw):
     return irregular_set(seed_insert, **kw), irregular_set(seed_query, **kw)
+
+
+def protein_like(seed_insert: int = 10, seed_query: int = 11, total: int = 500_000_000,
+                 median: float = 300.0, sigma: float = 0.6, frag_len: int = 50):
+    """Protein stand-in: `total` residues uniform over AMINO20 in log-normal
+    proteins; fragments of frag_len residues, half from the proteins at 1 %
+    substitution, half uniform."""
+    rng = _rng(seed_insert)
+    n = max(1, int(total / (median * np.exp(sigma * sigma / 2))))
+    lengths = np.clip(np.rint(lognormal_lengths(rng, n, median, sigma)), 30, 5_000).astype(np.int64)
+    lengths = lengths[np.cumsum(lengths) <= total]
+    if lengths.sum() < total:
+        lengths = np.append(lengths, total - lengths.sum())
+    seq = uniform_bases(rng, total, AMINO20)
+    ins = Workload(seq, csr(lengths), f"protein-like insert: {total:,} residues in {lengths.size:,} proteins")
+    n_frag = total // frag_len
+    frags, off, is_random = sample_reads(_rng(seed_query), ins.seq, ins.offsets, n_frag // 2,
+                                         n_frag - n_frag // 2, frag_len, 0.01, AMINO20)
+    qry = Workload(frags, off, f"protein-like query: {n_frag:,} fragments x {frag_len} residues",
+                   is_random=is_random)
+    return ins, qry
+
+
+def random_protein_records(rng: np.random.Generator, n_records: int, min_len: int, max_len: int,
+                           lower_prob: float = 0.0, junk_prob: float = 0.0):
+    """Small mixed protein inputs: uniform over all 26 letters, optional
+    lowercase letters and other bytes (stop '*', gap '-', digits, controls)."""
+    lengths = rng.integers(min_len, max_len + 1, size=n_records)
+    off = csr(lengths)
+    letters = np.arange(ord("A"), ord("Z") + 1, dtype=np.uint8)
+    seq = uniform_bases(rng, int(off[-1]), letters)
+    if lower_prob:
+        low = rng.random(seq.size) < lower_prob
+        seq[low] |= 0x20
+    if junk_prob:
+        junk = rng.random(seq.size) < junk_prob
+        seq[junk] = rng.choice(np.frombuffer(b"*-.019@[`{\x00\xff\xc1\xe1", dtype=np.uint8),
+                               size=int(junk.sum()))
+    return Workload(seq, off, "random mixed protein records")
 
 
 def random_records(rng: np.random.Generator, n_records: int, min_len: int, max_len: int,

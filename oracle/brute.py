@@ -1,5 +1,9 @@
 """Pure-Python brute force of SBF insert/query, for tiny inputs only.
 
+Alphabets (Sec. IV-A): "dna" (one base per symbol, radix 4), "protein" (one
+letter per symbol, A..Z = 0..25, radix 32) and "dna_triplet" (one codon of
+three bases per symbol, read in frame from the record start, radix 64).
+
 TEST INFRASTRUCTURE ONLY.  Written independently of ``sbf_oracle.c`` (Python
 strings and integers, no shared code) so that the two can pin each other.
 
@@ -20,12 +24,35 @@ C2 = 0x6A09E667F3BCC909
 _DIGIT = {"A": "0", "C": "1", "G": "2", "T": "3"}
 
 
-def kmer_value(text: str) -> int:
-    """Base-4 number whose first digit is the first base (A0 C1 G2 T3)."""
-    return int("".join(_DIGIT[ch] for ch in text.upper()), 4)
+_LETTERS = "ABCDEFGHIJKLMNOPQRSTUVWXYZ"
+# radix and input characters per symbol
+_SHAPE = {"dna": (4, 1), "protein": (32, 1), "dna_triplet": (64, 3)}
 
 
-def is_valid(text: str) -> bool:
+def symbols(text: str, alphabet: str = "dna"):
+    """The symbol codes of text (length a multiple of the symbol's width)."""
+    _, width = _SHAPE[alphabet]
+    if alphabet == "protein":
+        return [_LETTERS.index(ch.upper()) for ch in text]
+    if alphabet == "dna_triplet":
+        return [int("".join(_DIGIT[ch] for ch in text[i:i + 3].upper()), 4)
+                for i in range(0, len(text), width)]
+    return [int(_DIGIT[ch.upper()]) for ch in text]
+
+
+def kmer_value(text: str, alphabet: str = "dna") -> int:
+    """The symbols as digits of one number, first symbol most significant
+    (DNA: base 4 with A0 C1 G2 T3)."""
+    radix, _ = _SHAPE[alphabet]
+    v = 0
+    for c in symbols(text, alphabet):
+        v = v * radix + c
+    return v
+
+
+def is_valid(text: str, alphabet: str = "dna") -> bool:
+    if alphabet == "protein":
+        return all(ch.upper() in _LETTERS and ch.isascii() for ch in text)
     return all(ch in "ACGTacgt" for ch in text)
 
 
@@ -65,13 +92,16 @@ def smer_words(h: int, H: int):
     return words
 
 
-def kmer(text: str, k: int, m: int, s: int, H: int, num_shards: int, seed: int):
-    """(shard, words) of one valid k-mer given as a string of length k."""
-    minimizer = min(hm(kmer_value(text[i:i + m]), seed) for i in range(k - m + 1))
+def kmer(text: str, k: int, m: int, s: int, H: int, num_shards: int, seed: int,
+         alphabet: str = "dna"):
+    """(shard, words) of one valid k-mer given as its k symbols' characters."""
+    _, cw = _SHAPE[alphabet]
+    minimizer = min(hm(kmer_value(text[cw * i:cw * (i + m)], alphabet), seed)
+                    for i in range(k - m + 1))
     shard = minimizer % num_shards
     words = [0, 0, 0, 0]
     for j in range(k - s + 1):
-        for w, bits in enumerate(smer_words(hs(kmer_value(text[j:j + s]), seed), H)):
+        for w, bits in enumerate(smer_words(hs(kmer_value(text[cw * j:cw * (j + s)], alphabet), seed), H)):
             words[w] |= bits
     return shard, words
 
@@ -81,30 +111,36 @@ def records_of(seq: bytes, offsets):
             for r in range(len(offsets) - 1)]
 
 
-def insert(seq: bytes, offsets, k, m, s, H, num_shards, seed, filt=None):
+def kmers_of(rec: str, k: int, alphabet: str = "dna"):
+    """(offset in the record, characters) of every k-mer of one record: one
+    per symbol, symbols read in frame from the record's start."""
+    _, cw = _SHAPE[alphabet]
+    for p in range(0, len(rec) - cw * k + 1, cw):
+        yield p, rec[p:p + cw * k]
+
+
+def insert(seq: bytes, offsets, k, m, s, H, num_shards, seed, filt=None, alphabet: str = "dna"):
     """Return {shard: [w0, w1, w2, w3]} with every valid k-mer inserted."""
     filt = {} if filt is None else filt
     for _, rec in records_of(seq, offsets):
-        for p in range(len(rec) - k + 1):
-            text = rec[p:p + k]
-            if not is_valid(text):
+        for p, text in kmers_of(rec, k, alphabet):
+            if not is_valid(text, alphabet):
                 continue
-            shard, words = kmer(text, k, m, s, H, num_shards, seed)
+            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet)
             cur = filt.setdefault(shard, [0, 0, 0, 0])
             for w in range(4):
                 cur[w] |= words[w]
     return filt
 
 
-def query(filt, seq: bytes, offsets, k, m, s, H, num_shards, seed):
+def query(filt, seq: bytes, offsets, k, m, s, H, num_shards, seed, alphabet: str = "dna"):
     """Return the set of absolute positions whose k-mer answers present."""
     hits = set()
     for start, rec in records_of(seq, offsets):
-        for p in range(len(rec) - k + 1):
-            text = rec[p:p + k]
-            if not is_valid(text):
+        for p, text in kmers_of(rec, k, alphabet):
+            if not is_valid(text, alphabet):
                 continue
-            shard, words = kmer(text, k, m, s, H, num_shards, seed)
+            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet)
             have = filt.get(shard, [0, 0, 0, 0])
             if all((words[w] & ~have[w]) == 0 for w in range(4)):
                 hits.add(start + p)

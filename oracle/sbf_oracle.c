@@ -1,6 +1,6 @@
 /*
  * sbf_oracle.c -- plain, slow CPU oracle for Super Bloom filter (SBF)
- * insert and query over raw DNA.
+ * insert and query over raw DNA, protein and DNA-triplet sequences.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this file; only the tests, the package smoke check and the benchmark's
@@ -30,8 +30,17 @@
  * Readings where the paper leaves a step open (each one is listed in the
  * design notes):
  *   - code map A/a=0, C/c=1, G/g=2, T/t=3; every other byte is invalid;
- *   - a t-mer packs with its first base most significant (Sec. IV-E's
- *     "left-shift, OR in the trailing symbol");
+ *   - protein symbols are the 26 letters, either case, A/a=0 .. Z/z=25;
+ *     every other byte is invalid;
+ *   - a DNA-triplet symbol is three consecutive bases read in frame from the
+ *     start of its record, code 16*c0 + 4*c1 + c2 (the three 2-bit codes,
+ *     first base most significant); a codon holding an invalid base is
+ *     invalid, and the 1 or 2 bytes after a record's last whole codon start
+ *     no symbol.  A triplet k-mer therefore starts only at record-relative
+ *     byte offsets divisible by 3 and covers 3k bytes; its answer goes to the
+ *     bit of its first byte, the other bits are 0;
+ *   - a t-mer packs with its first symbol most significant (Sec. IV-E's
+ *     "left-shift, OR in the trailing symbol"), b bits per symbol;
  *   - hash constants: C1 = floor(2^64 / golden ratio), C2 = floor((sqrt2-1)
  *     * 2^64) | 1; minimizer hash hm(x) = t ^ (t >> 32) with
  *     t = (x ^ seed) * C1; s-mer hash hs(x): t = (x ^ ~seed) * C1,
@@ -78,6 +87,50 @@ uint64_t orc_pack(const uint8_t *p, int t)
     uint64_t v = 0;
     for (int i = 0; i < t; i++)
         v = v * 4u + (uint64_t)orc_base_code(p[i]);
+    return v;
+}
+
+/* Sec. IV-A alphabets: bits per symbol and input bytes per symbol. */
+enum { ORC_DNA = 0, ORC_PROTEIN = 1, ORC_TRIPLET = 2 };
+
+int orc_symbol_bits(int alphabet)
+{
+    return alphabet == ORC_PROTEIN ? 5 : alphabet == ORC_TRIPLET ? 6 : 2;
+}
+
+int orc_symbol_bytes(int alphabet)
+{
+    return alphabet == ORC_TRIPLET ? 3 : 1;
+}
+
+/* Code of the symbol whose first byte is p, or -1 when it is invalid. */
+int orc_symbol_code(int alphabet, const uint8_t *p)
+{
+    if (alphabet == ORC_PROTEIN) {
+        if (p[0] >= 'A' && p[0] <= 'Z')
+            return p[0] - 'A';
+        if (p[0] >= 'a' && p[0] <= 'z')
+            return p[0] - 'a';
+        return -1;
+    }
+    if (alphabet == ORC_TRIPLET) {
+        int c0 = orc_base_code(p[0]), c1 = orc_base_code(p[1]), c2 = orc_base_code(p[2]);
+        if (c0 < 0 || c1 < 0 || c2 < 0)
+            return -1;
+        return c0 * 16 + c1 * 4 + c2;
+    }
+    return orc_base_code(p[0]);
+}
+
+/* Packed value of the t symbols starting at p (symbol i at byte
+ * i * bytes-per-symbol), first symbol most significant:
+ * sum_i code_i * 2^(b*(t-1-i)).  The caller guarantees validity. */
+uint64_t orc_pack_symbols(int alphabet, const uint8_t *p, int t)
+{
+    const int b = orc_symbol_bits(alphabet), B = orc_symbol_bytes(alphabet);
+    uint64_t v = 0;
+    for (int i = 0; i < t; i++)
+        v = (v << b) | (uint64_t)orc_symbol_code(alphabet, p + (size_t)i * B);
     return v;
 }
 
@@ -133,33 +186,38 @@ typedef struct {
     int k, m, s, H;
     uint64_t num_shards; /* a power of two */
     uint64_t seed;
+    int alphabet;
 } orc_params;
 
 /* One k-mer, from scratch.  seq is the whole concatenated buffer, g an
- * absolute position, rec_end the end of g's record.  Returns 1 and fills
- * shard/K when the k-mer is valid (all k bases valid, inside the record). */
-static int kmer_info(const uint8_t *seq, int64_t g, int64_t rec_end,
+ * absolute position, [rec_start, rec_end) the byte range of g's record.
+ * Returns 1 and fills shard/K when the k-mer is valid: it starts on a symbol
+ * boundary of its record, its k symbols lie inside the record and all are
+ * valid (Sec. IV-F). */
+static int kmer_info(const uint8_t *seq, int64_t g, int64_t rec_start, int64_t rec_end,
                      const orc_params *P, uint64_t *shard, uint64_t K[4])
 {
-    const int k = P->k, m = P->m, s = P->s;
-    if (g + k > rec_end)
+    const int k = P->k, m = P->m, s = P->s, A = P->alphabet;
+    const int B = orc_symbol_bytes(A);
+    if ((g - rec_start) % B != 0 || g + (int64_t)B * k > rec_end)
         return 0;
     for (int i = 0; i < k; i++)
-        if (orc_base_code(seq[g + i]) < 0)
+        if (orc_symbol_code(A, seq + g + (int64_t)B * i) < 0)
             return 0;
-    /* Algorithm 1 lines 5-9: minimum hash over the k-m+1 m-mer windows. */
+    /* Algorithm 1: the minimizer is the minimum hash over the k-m+1 m-mer
+     * windows ... */
     uint64_t mu = UINT64_MAX;
     for (int i = 0; i <= k - m; i++) {
-        uint64_t h = orc_hash_m(orc_pack(seq + g + i, m), P->seed);
+        uint64_t h = orc_hash_m(orc_pack_symbols(A, seq + g + (int64_t)B * i, m), P->seed);
         if (h < mu)
             mu = h;
     }
-    /* Algorithm 1 line 10: shard = minHash & (NumShards - 1). */
+    /* ... its low bits select the shard (minHash & (NumShards - 1)) ... */
     *shard = mu & (P->num_shards - 1);
-    /* Algorithm 1 lines 11-14: OR the bits of all k-s+1 s-mers. */
+    /* ... and the bits of all k-s+1 s-mers are OR-ed into four word masks. */
     K[0] = K[1] = K[2] = K[3] = 0;
     for (int j = 0; j <= k - s; j++)
-        orc_smer_bits(orc_hash_s(orc_pack(seq + g + j, s), ~P->seed), P->H, K);
+        orc_smer_bits(orc_hash_s(orc_pack_symbols(A, seq + g + (int64_t)B * j, s), ~P->seed), P->H, K);
     return 1;
 }
 
@@ -198,7 +256,7 @@ static void *insert_worker(void *arg)
         while (J->off[r + 1] <= g)
             r++;
         uint64_t shard, K[4];
-        if (!kmer_info(J->seq, g, J->off[r + 1], &J->P, &shard, K))
+        if (!kmer_info(J->seq, g, J->off[r], J->off[r + 1], &J->P, &shard, K))
             continue;
         for (int w = 0; w < 4; w++) {
             if (!K[w])
@@ -223,7 +281,7 @@ static void *query_worker(void *arg)
             r++;
         uint64_t shard, K[4];
         int present = 0;
-        if (kmer_info(J->seq, g, J->off[r + 1], &J->P, &shard, K)) {
+        if (kmer_info(J->seq, g, J->off[r], J->off[r + 1], &J->P, &shard, K)) {
             /* Algorithm 2: present iff every required bit is set. */
             present = 1;
             for (int w = 0; w < 4; w++)
@@ -238,7 +296,11 @@ static void *query_worker(void *arg)
 
 static int valid_params(const orc_params *P)
 {
-    if (P->k < 1 || P->k > 32 || P->m < 1 || P->m > P->k || P->s < 1 || P->s > P->k)
+    if (P->alphabet < ORC_DNA || P->alphabet > ORC_TRIPLET)
+        return 0;
+    /* Sec. IV-C: a k-mer packs into one 64-bit word. */
+    if (P->k < 1 || P->k * orc_symbol_bits(P->alphabet) > 64 || P->m < 1 || P->m > P->k ||
+        P->s < 1 || P->s > P->k)
         return 0;
     if (P->H < 1 || P->H > 32)
         return 0;
@@ -305,10 +367,10 @@ static int check_offsets(const int64_t *off, int64_t n)
  * caller-zeroed or holding an earlier image.  Returns 0, or -1 on bad
  * arguments. */
 int orc_insert(uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t n,
-               int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+               int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
                int nthreads)
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     if (n == 0)
@@ -321,10 +383,10 @@ int orc_insert(uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t
  * [off[0]>>5, (off[n]+31)>>5); the words are zeroed here and bit g is set iff
  * the k-mer at absolute position g is valid and present. */
 int orc_query(const uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t n,
-              int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+              int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
               uint32_t *out, int nthreads)
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     if (n == 0)
@@ -338,34 +400,36 @@ int orc_query(const uint64_t *filter, const uint8_t *seq, const int64_t *off, in
 /* The k-mer at absolute position g (one record lookup, then from scratch).
  * Returns 1 if valid (shard and K filled), 0 if not, -1 on bad arguments. */
 int orc_kmer_info(const uint8_t *seq, const int64_t *off, int64_t n, int64_t g,
-                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
                   uint64_t *shard, uint64_t K[4])
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || n <= 0 || g < off[0] || g >= off[n])
         return -1;
     int64_t r = record_of(off, n, g);
-    return kmer_info(seq, g, off[r + 1], &P, shard, K);
+    return kmer_info(seq, g, off[r], off[r + 1], &P, shard, K);
 }
 
 /* Fig. 3 structure: counts valid k-mers and runs, a run being a maximal
- * stretch of consecutive valid k-mers of one record with one shard.  The
+ * stretch of consecutive valid k-mers of one record with one shard
+ * (consecutive: one symbol apart).  The
  * paper's insert issues one atomicOr per non-zero word per run; *atomics
  * receives that count.  Single-threaded, from scratch per k-mer. */
 int orc_count_runs(const uint8_t *seq, const int64_t *off, int64_t n,
-                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
                    int64_t *valid_kmers, int64_t *runs, int64_t *atomics)
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     int64_t nv = 0, nr = 0, na = 0;
     for (int64_t r = 0; r < n; r++) {
         int have = 0;
         uint64_t cur = 0, acc[4] = {0, 0, 0, 0};
-        for (int64_t g = off[r]; g < off[r + 1]; g++) {
+        /* consecutive k-mers of a record are one symbol apart */
+        for (int64_t g = off[r]; g < off[r + 1]; g += orc_symbol_bytes(alphabet)) {
             uint64_t shard, K[4];
-            int v = kmer_info(seq, g, off[r + 1], &P, &shard, K);
+            int v = kmer_info(seq, g, off[r], off[r + 1], &P, &shard, K);
             if (v && have && shard == cur) {
                 for (int w = 0; w < 4; w++)
                     acc[w] |= K[w];
@@ -400,10 +464,10 @@ int orc_count_runs(const uint8_t *seq, const int64_t *off, int64_t n,
  * arguments. */
 int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
                    const int64_t *pos, int64_t count,
-                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
                    uint8_t *valid, uint64_t *shard, uint64_t *K)
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || n <= 0)
         return -1;
     for (int64_t i = 0; i < count; i++) {
@@ -414,7 +478,7 @@ int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
         if (g < off[0] || g >= off[n])
             continue;
         int64_t r = record_of(off, n, g);
-        valid[i] = (uint8_t)kmer_info(seq, g, off[r + 1], &P, &shard[i], &K[4 * i]);
+        valid[i] = (uint8_t)kmer_info(seq, g, off[r], off[r + 1], &P, &shard[i], &K[4 * i]);
     }
     return 0;
 }
@@ -423,16 +487,16 @@ int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
  * sparse image.  rows must hold one entry per k-mer position; *count
  * receives the number of valid k-mers written. */
 int orc_kmer_rows(const uint8_t *seq, const int64_t *off, int64_t n,
-                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed,
+                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
                   uint64_t *shard, uint64_t *K, int64_t *count)
 {
-    orc_params P = {k, m, s, H, num_shards, seed};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     int64_t c = 0;
     for (int64_t r = 0; r < n; r++)
         for (int64_t g = off[r]; g < off[r + 1]; g++)
-            if (kmer_info(seq, g, off[r + 1], &P, &shard[c], &K[4 * c]))
+            if (kmer_info(seq, g, off[r], off[r + 1], &P, &shard[c], &K[4 * c]))
                 c++;
     *count = c;
     return 0;
