@@ -1,5 +1,6 @@
 /*
- * sbf.h -- C ABI of libsbf, a GB300 (sm_103a) Super Bloom filter for raw DNA.
+ * sbf.h -- C ABI of libsbf, a GB300 (sm_103a) Super Bloom filter for raw DNA
+ * (and, through sbf_create_alphabet, protein and DNA-triplet sequences).
  *
  * The method is the one of "cuSBF: A Minimizer-Aware Bloom Filter for Genomic
  * Sequence Data on Modern GPUs" (Dortmann, Vieth, Schmidt):
@@ -74,6 +75,32 @@ typedef enum {
  * seed selects the hash functions (minimizer seed = seed, s-mer seed = ~seed).
  * Returns NULL on error (SBF_ERR_INVALID_ARG / _OOM / _CUDA in sbf_last_error). */
 sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed);
+
+/* Sec. IV-A alphabet encodings. */
+#define SBF_ALPHABET_DNA 0         /* 4 symbols, 2 bits: A/a C/c G/g T/t = 0..3; k <= 32 */
+#define SBF_ALPHABET_PROTEIN 1     /* 26 symbols, 5 bits: letters A..Z, either case = 0..25; k <= 12 */
+#define SBF_ALPHABET_DNA_TRIPLET 2 /* 64 symbols, 6 bits: codons, 3 bytes each; k <= 10 */
+
+/* sbf_create for any of the three alphabets of Sec. IV-A (sbf_create is this
+ * call with SBF_ALPHABET_DNA).  A k-mer packs into one 64-bit word (Sec.
+ * IV-C), so k * bits-per-symbol <= 64: k <= 32 (DNA), 12 (protein), 10
+ * (triplet); 1 <= m <= k, 1 <= s <= k, 1 <= H <= 32 as for sbf_create.
+ *   - Protein: any byte other than a letter is an invalid symbol.
+ *   - DNA triplet: a symbol is a codon of three bases read in frame from the
+ *     start of its record, code 16*c0 + 4*c1 + c2 (2-bit base codes, first
+ *     base most significant); a codon holding an invalid base is invalid; the
+ *     1 or 2 bytes after a record's last whole codon start no symbol.
+ * The packed value of a t-mer is sum_i code_i * 2^(b*(t-1-i)), b the symbol
+ * width; hashing, sharding and bit addressing are those of sbf_create.  Insert
+ * and query keep their contracts with "position" meaning a byte of the
+ * concatenated input: the k-mer starting at a symbol's first byte g answers at
+ * bit g, and (triplets) bits of other bytes are 0.  These filters always run
+ * the runtime-parameter alphabet kernel (sbf_is_specialized returns 0).
+ * Returns NULL on error, like sbf_create. */
+sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet);
+
+/* The filter's alphabet (SBF_ALPHABET_*), or -1 for NULL. */
+int sbf_get_alphabet(const sbf_filter *f);
 
 /* Free the device memory of f after the device finished all work (this call
  * synchronizes the device).  NULL-safe. */

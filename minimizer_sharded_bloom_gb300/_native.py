@@ -22,6 +22,8 @@ _vp, _u64, _i64, _i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int64, ctypes
 _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "sbf_create": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64]),
+    "sbf_create_alphabet": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64, _i32]),
+    "sbf_get_alphabet": (_i32, [_vp]),
     "sbf_destroy": (None, [_vp]),
     "sbf_insert": (_i32, [_vp, _vp, _vp, _i64, _vp]),
     "sbf_query": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
@@ -151,6 +153,32 @@ def sbf_clear(f: int, stream: int = 0) -> None:
 
 def sbf_num_shards(f: int) -> int:
     return int(load().sbf_num_shards(f))
+
+
+# Sec. IV-A alphabets (SBF_ALPHABET_* of sbf.h)
+ALPHABET_DNA, ALPHABET_PROTEIN, ALPHABET_DNA_TRIPLET = 0, 1, 2
+ALPHABETS = {"dna": ALPHABET_DNA, "protein": ALPHABET_PROTEIN, "dna_triplet": ALPHABET_DNA_TRIPLET,
+             "triplet": ALPHABET_DNA_TRIPLET}
+
+
+def alphabet_id(alphabet) -> int:
+    if isinstance(alphabet, str):
+        try:
+            return ALPHABETS[alphabet.lower()]
+        except KeyError:
+            raise ValueError(f"unknown alphabet {alphabet!r}") from None
+    return int(alphabet)
+
+
+def sbf_create_alphabet(num_bits: int, k: int, m: int, s: int, H: int, seed: int, alphabet) -> int:
+    h = load().sbf_create_alphabet(num_bits, k, m, s, H, seed & (2**64 - 1), alphabet_id(alphabet))
+    if not h:
+        raise SBFError(SBF_ERR_INVALID_ARG, "sbf_create_alphabet", last_error())
+    return h
+
+
+def sbf_get_alphabet(f: int) -> int:
+    return int(load().sbf_get_alphabet(f))
 
 
 def sbf_get_params(f: int):

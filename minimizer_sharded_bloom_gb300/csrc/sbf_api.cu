@@ -170,13 +170,23 @@ extern "C" {
 const char *sbf_last_error(void) { return g_last_error.c_str(); }
 
 sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed) {
+    return sbf_create_alphabet(num_bits, k, m, s, H, seed, SBF_ALPHABET_DNA);
+}
+
+sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet) {
     g_last_error.clear();
     if (num_bits < 1) {
         fail(SBF_ERR_INVALID_ARG, "num_bits must be >= 1");
         return nullptr;
     }
-    if (k < 1 || k > 32 || m < 1 || m > k || s < 1 || s > k) {
-        fail(SBF_ERR_INVALID_ARG, "need 1 <= m <= k <= 32 and 1 <= s <= k (k=%d m=%d s=%d)", k, m, s);
+    if (alphabet < SBF_ALPHABET_DNA || alphabet > SBF_ALPHABET_DNA_TRIPLET) {
+        fail(SBF_ERR_INVALID_ARG, "unknown alphabet %d", alphabet);
+        return nullptr;
+    }
+    // Sec. IV-C: a k-mer packs into one 64-bit word
+    const int kmax = alphabet == SBF_ALPHABET_PROTEIN ? 12 : alphabet == SBF_ALPHABET_DNA_TRIPLET ? 10 : 32;
+    if (k < 1 || k > kmax || m < 1 || m > k || s < 1 || s > k) {
+        fail(SBF_ERR_INVALID_ARG, "need 1 <= m <= k <= %d and 1 <= s <= k (k=%d m=%d s=%d)", kmax, k, m, s);
         return nullptr;
     }
     if (H < 1 || H > sbf::kMaxH) {
@@ -195,6 +205,7 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
     f->m = m;
     f->s = s;
     f->H = H;
+    f->alphabet = alphabet;
     f->seed = seed;
     f->num_shards = shards;
     cudaError_t e = cudaGetDevice(&f->device);
@@ -225,7 +236,11 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
     const void *ins = nullptr, *qry = nullptr;
     int threads = 0;
     // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
-    if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
+    if (alphabet != SBF_ALPHABET_DNA) {
+        ins = sbf::alphabet_insert_kernel(alphabet);
+        qry = sbf::alphabet_query_kernel(alphabet);
+        threads = 256;
+    } else if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
     } else {
         ins = sbf::generic_insert_kernel();
@@ -267,6 +282,8 @@ int sbf_get_params(const sbf_filter *f, int *k, int *m, int *s, int *H, uint64_t
 }
 
 int sbf_is_specialized(const sbf_filter *f) { return f && f->specialized ? 1 : 0; }
+
+int sbf_get_alphabet(const sbf_filter *f) { return f ? f->alphabet : -1; }
 
 int sbf_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream) {
     if (!f || !seq || !offsets || n < 0) return fail(SBF_ERR_INVALID_ARG, "sbf_insert: bad arguments");

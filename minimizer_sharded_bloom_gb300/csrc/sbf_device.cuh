@@ -14,6 +14,8 @@ namespace sbf {
 constexpr uint64_t kC1 = 0x9E3779B97F4A7C15ull;  // floor(2^64 / golden ratio)
 constexpr uint64_t kC2 = 0x6A09E667F3BCC909ull;  // floor((sqrt(2) - 1) * 2^64) | 1
 constexpr int kStatusBadOffsets = 1;
+// Sec. IV-A alphabets (the values of SBF_ALPHABET_* in sbf.h)
+constexpr int kAlphabetDNA = 0, kAlphabetProtein = 1, kAlphabetTriplet = 2;
 constexpr int kStatusTimeout = 2;  // a bounded device wait gave up
 
 // Everything a kernel launch needs; passed by value (kernel parameter space).
@@ -76,17 +78,66 @@ __constant__ const uint64_t kSalt[kMaxH] = {
 // OR the H bits of one s-mer hash into four word masks (Sec. IV-B: hash i ->
 // word i mod 4).  Sec. IV-G: bit-slicing with slice width floor(64/H) while it
 // is at least 6 bits; beyond, the top 6 bits of hs * salt(i).
+// (Loops unrolled to their bounds so that K stays in registers.)
 __device__ __forceinline__ void smer_bits_runtime(uint64_t hs, int H, uint64_t K[4]) {
     const int W = 64 / H;
     if (W >= 6) {
-        for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);
+#pragma unroll
+        for (int i = 0; i < 10; ++i)
+            if (i < H) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);
     } else {
-        for (int i = 0; i < H; ++i) K[i & 3] |= 1ull << ((hs * kSalt[i]) >> 58);
+        // groups of four hashes: word q of the group is constant per unrolled step
+#pragma unroll 1
+        for (int i0 = 0; i0 < H; i0 += 4)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i0 + q < H) K[q] |= 1ull << ((hs * kSalt[i0 + q]) >> 58);
     }
 }
 
 __device__ __forceinline__ uint64_t low_mask(int symbols) {
     return symbols >= 32 ? ~0ull : ((1ull << (2 * symbols)) - 1ull);
+}
+
+// First record boundary r in [0, n] with offsets[r] > x (n + 1 if none), by
+// one warp: an interpolation probe of 32 consecutive boundaries around the
+// guess for evenly sized records, then 32-way searches (one load round each).
+__device__ __forceinline__ int64_t warp_find_boundary(const int64_t *off, int64_t n, int64_t x, int64_t lo,
+                                                      int64_t hi, int lane) {
+    int64_t r_lo = 0, r_hi = n + 1;  // offsets[r] <= x for r < r_lo; > x for r >= r_hi
+    {
+        const double frac = hi > lo ? (double)(x - lo) / (double)(hi - lo) : 0.0;
+        int64_t g = (int64_t)(frac * (double)n);
+        g = g < 0 ? 0 : (g > n ? n : g);
+        int64_t p = g - 15 + lane;
+        p = p < 0 ? 0 : (p > n ? n : p);
+        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
+        const int64_t p31 = __shfl_sync(0xffffffffu, p, 31);
+        if (b == 0) {
+            r_lo = p31 + 1;
+        } else {
+            const int f = __ffs(b) - 1;
+            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
+            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
+            r_hi = pf;
+            if (f > 0) r_lo = pf1 + 1;
+        }
+    }
+    while (r_lo < r_hi) {
+        const int64_t span = r_hi - r_lo;
+        const int64_t p = r_lo + (span * lane) / 32;
+        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
+        if (b == 0) {
+            r_lo = __shfl_sync(0xffffffffu, p, 31) + 1;
+        } else {
+            const int f = __ffs(b) - 1;
+            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
+            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
+            r_hi = pf;
+            if (f > 0) r_lo = pf1 + 1;
+        }
+    }
+    return r_lo;
 }
 
 }  // namespace sbf

@@ -3,11 +3,12 @@
 // staging and host-to-device copies with kernels on alternating streams).
 //
 // The CSR batch is cut into chunks of output positions [cs, ce) (cs, ce
-// multiples of 32 except at the very end).  A chunk ships the bases
-// [max(cs, offsets[0]), min(ce + k - 1, offsets[n])) and its records clipped to
-// that range, so every k-mer that starts in [cs, ce) sees exactly its own
-// bases; k-mers starting at or after ce fall off the clipped end and are
-// invalid in that chunk.  Chunk c runs on slot c & 1 (a stream, device buffers
+// multiples of 32 except at the very end).  A chunk ships the bytes
+// [max(cs, offsets[0]), min(ce + kb - 1, offsets[n])) (kb = bytes of one
+// k-mer) and its records clipped to that range, so every k-mer that starts in
+// [cs, ce) sees exactly its own bytes; k-mers starting at or after ce fall off
+// the clipped end and are invalid in that chunk.  A record clipped at the
+// chunk's start keeps its symbol frame (DNA triplets).  Chunk c runs on slot c & 1 (a stream, device buffers
 // and pinned buffers, all kept in the filter between calls); the host prepares
 // chunk c+1 while the GPU works on chunk c.  Host buffers that are already
 // page-locked are copied from (and to) directly; pageable ones go through the
@@ -175,10 +176,15 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     for (int64_t c = 0; cs < hi && rc == SBF_OK; ++c) {
         const int64_t ce = std::min<int64_t>(cs + f->host_chunk, hi);
         const int64_t data_lo = std::max<int64_t>(cs, lo);
-        const int64_t data_hi = std::min<int64_t>(ce + f->k - 1, hi);
+        const int64_t data_hi = std::min<int64_t>(ce + sbf::kmer_bytes(f) - 1, hi);
         const int64_t r0 = record_at(off, n, data_lo);
         const int64_t r1 = record_at(off, n, data_hi - 1) + 1;
         const int64_t n_loc = r1 - r0;
+        // A record clipped at data_lo keeps its symbol frame: its chunk-local
+        // start moves up to its next symbol boundary (triplets; the bytes
+        // skipped start no symbol of the record).
+        const int sb = sbf::symbol_bytes(f->alphabet);
+        const int64_t first_lo = off[r0] < data_lo ? data_lo + (sb - (data_lo - off[r0]) % sb) % sb : data_lo;
         const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel writes
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
         Slot &s = st.slot[c & 1];
@@ -199,6 +205,8 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         cudaStreamWaitEvent(s.stream, ready, 0);
         for (int64_t r = 0; r <= n_loc; ++r)
             s.h_off[r] = std::min<int64_t>(std::max<int64_t>(off[r0 + r], data_lo), data_hi) - cs;
+        // (a record that ends before that boundary is left empty)
+        s.h_off[0] = std::min<int64_t>(first_lo - cs, s.h_off[1]);
         const char *src = seq + data_lo;
         char *dst = s.d_seq + (data_lo - cs);
         if (seq_kind == 0) {

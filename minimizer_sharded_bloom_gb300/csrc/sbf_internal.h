@@ -8,6 +8,7 @@
 struct sbf_filter {
     int device = 0;
     int k = 0, m = 0, s = 0, H = 0;
+    int alphabet = SBF_ALPHABET_DNA;
     uint64_t seed = 0;
     uint64_t num_shards = 0;
     uint64_t *words = nullptr;  // num_shards * 4 words
@@ -24,6 +25,10 @@ struct sbf_filter {
 };
 
 namespace sbf {
+// Input bytes per symbol of an alphabet (3 for DNA triplets, else 1).
+inline int symbol_bytes(int alphabet) { return alphabet == SBF_ALPHABET_DNA_TRIPLET ? 3 : 1; }
+// Bytes one k-mer of f covers.
+inline int64_t kmer_bytes(const sbf_filter *f) { return (int64_t)f->k * symbol_bytes(f->alphabet); }
 // Records the calling thread's error message and returns `code`.
 int set_error(int code, const char *fmt, ...);
 void destroy_stager(void *stager);

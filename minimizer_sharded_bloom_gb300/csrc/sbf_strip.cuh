@@ -18,7 +18,7 @@
 //    each m-mer and each s-mer is packed and hashed once, not once per k-mer
 //    that contains it.
 //
-//  * Minimizer (Algorithm 1 lines 5-9) with a Gil-Werman / van Herk sliding
+//  * Minimizer (Algorithm 1's minimum m-mer hash) with a Gil-Werman / van Herk sliding
 //    minimum: the m-mer hashes are cut into blocks of w = k-m+1; the minimum
 //    over a window is min(suffix-min of its first block, prefix-min of the
 //    next) -- three 64-bit minimums per k-mer instead of w-1.  Exact, so the
@@ -251,47 +251,6 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8]) {
         m[2 * (i & 3)] |= (uint32_t)one;
         m[2 * (i & 3) + 1] |= (uint32_t)(one >> 32);
     }
-}
-
-// First record boundary r in [0, n] with offsets[r] > x (n + 1 if none), by
-// one warp: an interpolation probe of 32 consecutive boundaries around the
-// guess for evenly sized records, then 32-way searches (one load round each).
-__device__ __forceinline__ int64_t warp_find_boundary(const int64_t *off, int64_t n, int64_t x, int64_t lo,
-                                                      int64_t hi, int lane) {
-    int64_t r_lo = 0, r_hi = n + 1;  // offsets[r] <= x for r < r_lo; > x for r >= r_hi
-    {
-        const double frac = hi > lo ? (double)(x - lo) / (double)(hi - lo) : 0.0;
-        int64_t g = (int64_t)(frac * (double)n);
-        g = g < 0 ? 0 : (g > n ? n : g);
-        int64_t p = g - 15 + lane;
-        p = p < 0 ? 0 : (p > n ? n : p);
-        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
-        const int64_t p31 = __shfl_sync(0xffffffffu, p, 31);
-        if (b == 0) {
-            r_lo = p31 + 1;
-        } else {
-            const int f = __ffs(b) - 1;
-            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
-            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
-            r_hi = pf;
-            if (f > 0) r_lo = pf1 + 1;
-        }
-    }
-    while (r_lo < r_hi) {
-        const int64_t span = r_hi - r_lo;
-        const int64_t p = r_lo + (span * lane) / 32;
-        const unsigned b = __ballot_sync(0xffffffffu, off[p] > x);
-        if (b == 0) {
-            r_lo = __shfl_sync(0xffffffffu, p, 31) + 1;
-        } else {
-            const int f = __ffs(b) - 1;
-            const int64_t pf = __shfl_sync(0xffffffffu, p, f);
-            const int64_t pf1 = __shfl_sync(0xffffffffu, p, f > 0 ? f - 1 : 0);
-            r_hi = pf;
-            if (f > 0) r_lo = pf1 + 1;
-        }
-    }
-    return r_lo;
 }
 
 template <int K, int M, int S, int H, bool kQuery>

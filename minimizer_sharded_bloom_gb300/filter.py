@@ -31,8 +31,11 @@ class SuperBloomFilter:
     """An SBF on the current CUDA device (sbf_create / sbf_destroy)."""
 
     def __init__(self, num_bits: int, k: int = 31, m: int = 16, s: int = 28, H: int = 4,
-                 seed: int = 0):
-        self._h = N.sbf_create(int(num_bits), k, m, s, H, seed)
+                 seed: int = 0, alphabet="dna"):
+        """alphabet: "dna" (default), "protein" or "dna_triplet" (Sec. IV-A;
+        k <= 32, 12, 10 respectively), or the SBF_ALPHABET_* value."""
+        self.alphabet = N.alphabet_id(alphabet)
+        self._h = N.sbf_create_alphabet(int(num_bits), k, m, s, H, seed, self.alphabet)
         self.k, self.m, self.s, self.H = k, m, s, H
         self.seed = seed & (2**64 - 1)
         self.num_shards = N.sbf_num_shards(self._h)

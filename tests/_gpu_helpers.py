@@ -48,16 +48,16 @@ def gpu_query(torch, sbf, seq, offsets, pad_front=0, sentinel=None):
     return out.cpu().numpy().view(np.uint32)
 
 
-def oracle_image(seq, offsets, params, num_bits, seed, nthreads=8):
+def oracle_image(seq, offsets, params, num_bits, seed, nthreads=8, alphabet="dna"):
     F = oracle.new_filter(num_bits)
     oracle.insert(F, seq, offsets, params["k"], params["m"], params["s"], params["H"], seed,
-                  nthreads=nthreads)
+                  nthreads=nthreads, alphabet=alphabet)
     return F
 
 
-def oracle_answers(F, seq, offsets, params, seed, nthreads=8):
+def oracle_answers(F, seq, offsets, params, seed, nthreads=8, alphabet="dna"):
     return oracle.query(F, seq, offsets, params["k"], params["m"], params["s"], params["H"], seed,
-                        nthreads=nthreads)
+                        nthreads=nthreads, alphabet=alphabet)
 
 
 def assert_words_equal(gpu_words, oracle_words, offsets):

@@ -1,0 +1,158 @@
+"""Parity of the protein and DNA-triplet kernels (through the C ABI) with the
+CPU oracle ("cuSBF", Sec. IV-A alphabets): bit-exact filter images and answer
+words on seeded inputs spanning many tiles with ragged tails, on the edge cases
+of the contract, and through the host-facing entry points with chunk edges
+that cut records inside a codon."""
+import numpy as np
+import pytest
+
+from minimizer_sharded_bloom_gb300 import synth
+from _gpu_helpers import (assert_images_equal, assert_words_equal, gpu_insert, gpu_query, need_gpu,
+                          oracle_answers, oracle_image, answer_bits)
+
+pytestmark = pytest.mark.gpu
+
+PROTEIN = dict(k=12, m=6, s=10, H=4)
+TRIPLET = dict(k=10, m=5, s=8, H=4)
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return need_gpu()
+
+
+def _filter(num_bits, params, seed, alphabet):
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter
+    f = SuperBloomFilter(num_bits, seed=seed, alphabet=alphabet, **params)
+    assert not f.specialized
+    return f
+
+
+def _records(rng, alphabet, n, lo, hi, dirty):
+    if alphabet == "protein":
+        return synth.random_protein_records(rng, n, lo, hi, lower_prob=0.05 * dirty,
+                                            junk_prob=0.002 * dirty)
+    return synth.random_records(rng, n, lo, hi, n_prob=0.002 * dirty, lower_prob=0.05 * dirty,
+                                junk_prob=0.0005 * dirty)
+
+
+def _roundtrip(torch, alphabet, ins, qry, params, num_bits, seed, pad_front=0):
+    sbf = _filter(num_bits, params, seed, alphabet)
+    gpu_insert(torch, sbf, ins.seq, ins.offsets, pad_front)
+    F = oracle_image(ins.seq, ins.offsets, params, num_bits, seed, alphabet=alphabet)
+    assert_images_equal(sbf.to_numpy(), F)
+    got = gpu_query(torch, sbf, qry.seq, qry.offsets, pad_front, sentinel=-1)
+    want = oracle_answers(F, qry.seq, qry.offsets, params, seed, alphabet=alphabet)
+    assert_words_equal(got, want, qry.offsets)
+    sbf.close()
+    return F, got
+
+
+def _with_own(ins, other):
+    """Query batch: the inserted records, then others."""
+    return synth.Workload(np.concatenate([ins.seq, other.seq]),
+                          np.concatenate([ins.offsets, ins.offsets[-1] + other.offsets[1:]]))
+
+
+@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
+def test_mixed_records_random_params(torch, alphabet, case):
+    """Random (k, m, s, H) within the 64-bit packing limit (H up to 32: the
+    salted multiply for H > 10), random shard counts, mixed records (invalid
+    symbols, lowercase, empty and short records, lengths not divisible by 3),
+    tens of tiles with a ragged tail, an unaligned sequence pointer for odd
+    cases."""
+    rng = np.random.default_rng(7000 + case + (0 if alphabet == "protein" else 100))
+    kmax = 12 if alphabet == "protein" else 10
+    k = int(rng.integers(1, kmax + 1))
+    params = dict(k=k, m=int(rng.integers(1, k + 1)), s=int(rng.integers(1, k + 1)),
+                  H=int(rng.integers(1, 11)) if case % 4 else int(rng.integers(11, 33)))
+    num_bits = int(2 ** rng.integers(8, 22))
+    ins = _records(rng, alphabet, int(rng.integers(1, 80)), 0, int(rng.integers(20, 6000)), case % 3)
+    qry = _with_own(ins, _records(rng, alphabet, int(rng.integers(1, 80)), 0, 3000, 1))
+    _roundtrip(torch, alphabet, ins, qry, params, num_bits, seed=int(rng.integers(0, 2**62)),
+               pad_front=case % 2 * 5)
+
+
+@pytest.mark.parametrize("alphabet,params", [("protein", PROTEIN), ("dna_triplet", TRIPLET)])
+def test_benchmark_params_long_records(torch, alphabet, params):
+    """The benchmark's parameters on long records (many tiles per record,
+    frame kept across tiles) and offsets[0] > 0, not a multiple of 32."""
+    rng = np.random.default_rng(71)
+    body = _records(rng, alphabet, 7, 20_000, 60_000, 1)
+    lead = 77
+    ins = synth.Workload(np.concatenate([np.full(lead, ord("A"), np.uint8), body.seq]),
+                         np.concatenate([[lead], lead + body.offsets[1:]]))
+    qry = _with_own(ins, _records(rng, alphabet, 300, 1, 400, 1))
+    F, got = _roundtrip(torch, alphabet, ins, qry, params, 1 << 22, seed=5)
+    # every inserted valid k-mer answers present
+    own = np.arange(lead, int(ins.offsets[-1]))
+    want = oracle_answers(F, ins.seq, ins.offsets, params, 5, alphabet=alphabet)
+    assert np.array_equal(answer_bits(got, own), answer_bits(want, own))
+
+
+@pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
+def test_edge_cases(torch, alphabet):
+    """n = 0 (no work, output untouched); only empty records; records shorter
+    than a k-mer; exactly one k-mer (3k bytes for triplets, +1 and +2 bytes);
+    k = m = s = 1; the maximum k; thousands of 1-4 byte records (many record
+    boundaries per tile)."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    kmax = 12 if alphabet == "protein" else 10
+    B = 1 if alphabet == "protein" else 3
+    sym = b"MKVLAQWERTYIPASDFGHCNY" if alphabet == "protein" else b"ACGTTGCAAGCTTCGA"
+    # n = 0
+    sbf = _filter(1 << 12, PROTEIN if alphabet == "protein" else TRIPLET, 1, alphabet)
+    seq = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    off = torch.zeros(1, dtype=torch.int64, device="cuda")
+    out = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    sbf.query(seq, off, out=out)
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy() == -1).all()
+    sbf.close()
+    rng = np.random.default_rng(72)
+    cases = []
+    cases.append(synth.Workload(np.zeros(0, np.uint8), synth.csr([0, 0, 0])))
+    text = (sym * 40)[: B * kmax + 2]
+    for extra in (-1, 0, 1, 2):
+        L = B * kmax + extra
+        cases.append(synth.Workload(np.frombuffer(text[:L], np.uint8).copy(), synth.csr([L])))
+    tiny = _records(rng, alphabet, 5000, 1, 4, 0)
+    cases.append(tiny)
+    for p in (dict(k=1, m=1, s=1, H=1), dict(k=kmax, m=kmax, s=kmax, H=32),
+              dict(k=kmax, m=1, s=1, H=7)):
+        for wl in cases:
+            _roundtrip(torch, alphabet, wl, wl, p, 1 << 10, seed=9)
+    assert N.sbf_get_alphabet(_filter(1 << 10, dict(k=3, m=2, s=2, H=2), 1, alphabet).handle) == \
+        N.alphabet_id(alphabet)
+
+
+@pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
+def test_create_rejects_k_beyond_packing(torch, alphabet):
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter, _native as N
+    kmax = 12 if alphabet == "protein" else 10
+    with pytest.raises(N.SBFError):
+        SuperBloomFilter(1 << 10, k=kmax + 1, m=2, s=2, H=2, alphabet=alphabet)
+    with pytest.raises(ValueError):
+        SuperBloomFilter(1 << 10, k=5, m=2, s=2, H=2, alphabet="rna")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("alphabet,params", [("protein", PROTEIN), ("dna_triplet", TRIPLET)])
+def test_host_entry_points(torch, alphabet, params, mode):
+    """sbf_insert_host / sbf_query_host in place (mode 0) and staged in chunks
+    of 4096 positions (mode 1): chunk edges cut records at every phase of
+    their codon frame, which each chunk must keep."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(73)
+    ins = _records(rng, alphabet, 30, 0, 5000, 1)
+    qry = _with_own(ins, _records(rng, alphabet, 50, 0, 900, 1))
+    sbf = _filter(1 << 16, params, 21, alphabet)
+    N.sbf_set_host_chunk(sbf.handle, 4096)
+    N.sbf_set_host_mode(sbf.handle, mode)
+    sbf.insert_host(ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, params, 1 << 16, 21, alphabet=alphabet)
+    assert_images_equal(sbf.to_numpy(), F)
+    out = sbf.query_host(qry.seq, qry.offsets)
+    assert_words_equal(out, oracle_answers(F, qry.seq, qry.offsets, params, 21, alphabet=alphabet),
+                       qry.offsets)

@@ -122,8 +122,9 @@ def test_hash_s_inverts():
 
 
 def test_hash_m_low_bits_depend_on_first_base():
-    """The shard uses the low bits of the minimizer hash (Algorithm 1,
-    line 10); they must change when only the first base of the m-mer does."""
+    """The shard uses the low bits of the minimizer hash (Algorithm 1's
+    minHash & (NumShards - 1)); they must change when only the first base of
+    the m-mer does."""
     seed = 0x1234
     changed = 0
     for tail in range(200):
