@@ -15,6 +15,9 @@ inside the timed region), the false-positive rate of the uniform reads, the
 roofline of the dominant kernel, SM clocks sampled during the timed region and
 the CPU oracle timed on the host cores.
 
+The protein-like and triplet workloads measure the other two alphabets of the
+paper's Sec. IV-A with their own parameters (stated in each workload).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle arm
 """
@@ -41,6 +44,24 @@ from minimizer_sharded_bloom_gb300 import synth  # noqa: E402
 METRIC = "k-mers/s insert & query (k=31,s=28,m=16,H=4); FPR; % HBM roofline"
 K, M, S, H = 31, 16, 28, 4
 SEED = 5
+MAIN = dict(k=K, m=M, s=S, H=H, alphabet="dna")
+# the other alphabets (Sec. IV-A): k at the 64-bit packing limit, s = k - 2
+# (three s-mers per k-mer); m = 8 for proteins (at m = 6 only 20^6 = 64 M
+# distinct m-mers exist, each recurring in a 500 M-residue set, and the
+# minimizers pile onto few shards: FPR 4 %), m = 5 for codons (64^5 m-mers)
+PROTEIN = dict(k=12, m=8, s=10, H=4, alphabet="protein")
+TRIPLET = dict(k=10, m=5, s=8, H=4, alphabet="dna_triplet")
+
+
+def metric_of(p):
+    if p == MAIN:
+        return METRIC
+    return (f"k-mers/s insert & query ({p['alphabet']}, k={p['k']},s={p['s']},m={p['m']},"
+            f"H={p['H']}); FPR; % roofline")
+
+
+def sym_bytes(p) -> int:
+    return 3 if p["alphabet"] == "dna_triplet" else 1
 
 WORKLOADS = {
     "out-of-cache": dict(bits=1 << 36, make=lambda: synth.out_of_cache(),
@@ -59,6 +80,24 @@ WORKLOADS = {
                            "runs of 1-50) into a 2^32-bit filter; query a disjoint equal set"),
     "tiny": dict(bits=1 << 20, make=lambda: synth.tiny(),
                  desc="tiny: 100 kbp into 2^20 bits; query it plus 100 kbp uniform"),
+    "protein-like": dict(bits=1 << 33, make=lambda: synth.protein_like(), p=PROTEIN,
+                         desc="protein-like: 500 M residues uniform over the 20 amino acids in "
+                              "log-normal proteins (median 300) into a 2^33-bit (1 GiB) filter; "
+                              "query 10,000,000 x 50-residue fragments (50% from the proteins at "
+                              "1% substitution, 50% uniform); protein alphabet, k=12 m=8 s=10 H=4"),
+    "protein-like-small": dict(bits=1 << 31, make=lambda: synth.protein_like(total=100_000_000),
+                               p=PROTEIN,
+                               desc="protein-like, profiling size: 100 M residues into a 2^31-bit "
+                                    "(256 MiB) filter; query 2,000,000 x 50-residue fragments"),
+    "triplet-small": dict(bits=1 << 31, make=lambda: synth.out_of_cache(total=200_000_000,
+                                                                         n_contigs=2_000),
+                          p=TRIPLET,
+                          desc="DNA triplets, profiling size: 200 Mbp in 2,000 contigs into a "
+                               "2^31-bit (256 MiB) filter; query 1,333,333 x 150 bp reads"),
+    "triplet": dict(bits=1 << 33, make=lambda: synth.out_of_cache(), p=TRIPLET,
+                    desc="DNA triplets: the out-of-cache data (1 Gbp in 10,000 contigs; "
+                         "6,666,666 x 150 bp reads) read as in-frame codons into a 2^33-bit "
+                         "(1 GiB) filter; triplet alphabet, k=10 m=5 s=8 H=4"),
 }
 
 # Algorithmic integer operations per k-mer of the rolling formulation
@@ -72,6 +111,13 @@ WORKLOADS = {
 # 9, answer bit 1).  The multiplies of the two hashes (11 per k-mer) run on
 # the FMA pipe and are not counted.
 ALU_OPS_PER_KMER = {"insert": 49, "query": 65}
+
+
+def alu_ops(p):
+    """The same count for any (k, s, alphabet): the k-mer mask costs 4 ops per
+    s-mer (k-s+1 of them); a codon decodes from three bases (+2)."""
+    front = 39 + (2 if p["alphabet"] == "dna_triplet" else 0)
+    return {"insert": front + 10, "query": front + 4 * (p["k"] - p["s"] + 1) + 10}
 # ALU-pipe peak: 152 SMs x 4 sub-partitions x 16 lanes x 2.07 GHz (maximum SM
 # clock).  ncu reports the ALU pipe at 16 lanes per sub-partition: with the
 # pipe ~75 % busy the issue rate is ~53 %, i.e. one ALU warp-instruction per
@@ -174,25 +220,26 @@ def throughput(world: int, steps: int, kmers_per_step: int, seconds: float) -> f
     return world * steps * kmers_per_step / seconds
 
 
-def kmer_count(wl, k=K):
-    return wl.kmer_positions(k)
+def kmer_count(wl, k=K, B=1):
+    """k-mer positions: per record floor(len / B) - k + 1 (B bytes per symbol)."""
+    return int(np.maximum(np.diff(wl.offsets) // B - k + 1, 0).sum())
 
 
-def runs_estimate(wl, k=K, m=M):
+def runs_estimate(wl, k=K, m=M, B=1):
     """Expected runs: density 2/(w+1) per k-mer (Sec. II-B1) plus one run
     start per record."""
     w = k - m + 1
-    return kmer_count(wl, k) * 2.0 / (w + 1) + wl.n_records
+    return kmer_count(wl, k, B) * 2.0 / (w + 1) + wl.n_records
 
 
-def fpr_count(qry, k=K) -> int:
+def fpr_count(qry, k=K, B=1) -> int:
     rnd = qry.meta.get("is_random")
     if rnd is None:
         return 0
-    return int(np.maximum(np.diff(qry.offsets)[rnd] - k + 1, 0).sum())
+    return int(np.maximum(np.diff(qry.offsets)[rnd] // B - k + 1, 0).sum())
 
 
-def fpr_of(words: np.ndarray, qry, k=K) -> float | None:
+def fpr_of(words: np.ndarray, qry, k=K, B=1) -> float | None:
     rnd = qry.meta.get("is_random")
     if rnd is None or not rnd.any():
         return None
@@ -201,17 +248,17 @@ def fpr_of(words: np.ndarray, qry, k=K) -> float | None:
     hits = total = 0
     for c in range(0, starts.size, 1 << 16):
         st, ln = starts[c:c + (1 << 16)], lens[c:c + (1 << 16)]
-        nk = np.maximum(ln - k + 1, 0)
+        nk = np.maximum(ln // B - k + 1, 0)
         if nk.sum() == 0:
             continue
-        pos = np.repeat(st, nk) + (np.arange(nk.sum()) - np.repeat(np.cumsum(nk) - nk, nk))
+        pos = np.repeat(st, nk) + B * (np.arange(nk.sum()) - np.repeat(np.cumsum(nk) - nk, nk))
         bits = (words[pos >> 5] >> (pos & 31).astype(np.uint32)) & 1
         hits += int(bits.sum())
         total += int(pos.size)
     return hits / total if total else None
 
 
-def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int = 300_000):
+def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int = 300_000, p=MAIN):
     """The CPU oracle, as it stands, on a bounded prefix sample of the same
     workload, all host cores."""
     import oracle
@@ -227,38 +274,42 @@ def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int
     s_q = synth.Workload(qry.seq[:qry.offsets[rq]], qry.offsets[:rq + 1])
     F = oracle.new_filter(bits)
     t0 = time.perf_counter()
-    oracle.insert(F, s_ins.seq, s_ins.offsets, K, M, S, H, SEED, nthreads=cores)
+    k, m, s, h, B = p["k"], p["m"], p["s"], p["H"], sym_bytes(p)
+    oracle.insert(F, s_ins.seq, s_ins.offsets, k, m, s, h, SEED, nthreads=cores, alphabet=p["alphabet"])
     t1 = time.perf_counter()
-    oracle.query(F, s_q.seq, s_q.offsets, K, M, S, H, SEED, nthreads=cores)
+    oracle.query(F, s_q.seq, s_q.offsets, k, m, s, h, SEED, nthreads=cores, alphabet=p["alphabet"])
     t2 = time.perf_counter()
-    nk = kmer_count(s_ins) + kmer_count(s_q)
+    nk_i, nk_q = kmer_count(s_ins, k, B), kmer_count(s_q, k, B)
+    nk = nk_i + nk_q
     return {"value": nk / (t2 - t0), "unit": "k-mers/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {s_ins.n_bases:,} bp ({r} records) inserted, first {rq:,} reads "
+            "sample": f"first {s_ins.n_bases:,} bytes ({r} records) inserted, first {rq:,} reads "
                       f"queried; {nk:,} k-mers in {t2 - t0:.1f} s",
-            "insert_kmers_per_s": kmer_count(s_ins) / (t1 - t0),
-            "query_kmers_per_s": kmer_count(s_q) / (t2 - t1)}
+            "insert_kmers_per_s": nk_i / (t1 - t0),
+            "query_kmers_per_s": nk_q / (t2 - t1)}
 
 
 def run_reference(args, workload):
     """The reference arm: the CPU oracle on the host cores, one bounded sample
     of the workload per step."""
     spec = WORKLOADS[workload]
+    p = spec.get("p", MAIN)
     ins, qry = spec["make"]()
     for _ in range(args.warmup):
-        cpu_baseline(ins, qry, spec["bits"], budget_bases=2_000_000, reads=20_000)
+        cpu_baseline(ins, qry, spec["bits"], budget_bases=2_000_000, reads=20_000, p=p)
     vals, secs = [], []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(ins, qry, spec["bits"], budget_bases=10_000_000, reads=100_000)
+        cb = cpu_baseline(ins, qry, spec["bits"], budget_bases=10_000_000, reads=100_000, p=p)
         secs.append(time.perf_counter() - t0)
         vals.append(cb["value"])
     value = float(np.mean(vals))
     cb["value"] = value
-    line = {"metric": METRIC, "value": value, "unit": "k-mers/s", "n_gpus": args.gpus,
+    line = {"metric": metric_of(p), "value": value, "unit": "k-mers/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": spec["desc"], "k": K, "m": M, "s": S, "H": H,
+            "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
+                       "alphabet": p["alphabet"],
                        "filter_bits": spec["bits"], "timing": "host wall clock per sample"},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "k-mers/s", "h2d_bytes_per_step": 0,
@@ -299,17 +350,24 @@ def main():
     torch.cuda.set_device(local)
     build_lib.build()
     spec = WORKLOADS[args.workload]
+    p = spec.get("p", MAIN)
+    B = sym_bytes(p)
     ins, qry = spec["make"]()
-    nk_ins, nk_q = kmer_count(ins), kmer_count(qry)
+    nk_ins, nk_q = kmer_count(ins, p["k"], B), kmer_count(qry, p["k"], B)
 
     dseq = torch.from_numpy(ins.seq).cuda()
     doff = torch.from_numpy(ins.offsets).cuda()
     dq = torch.from_numpy(qry.seq).cuda()
     dqo = torch.from_numpy(qry.offsets).cuda()
     out = torch.zeros((qry.n_bases + 31) // 32 + 1, dtype=torch.int32, device="cuda")
-    sbf = SuperBloomFilter(spec["bits"], k=K, m=M, s=S, H=H, seed=SEED)
-    if not sbf.specialized:
+    sbf = SuperBloomFilter(spec["bits"], k=p["k"], m=p["m"], s=p["s"], H=p["H"], seed=SEED,
+                           alphabet=p["alphabet"])
+    if p["alphabet"] == "dna" and not sbf.specialized:
         raise RuntimeError("the benchmark configuration must run its specialised kernel")
+    if p["alphabet"] == "dna":
+        kname = f"strip_kernel<{p['k']},{p['m']},{p['s']},{p['H']},%s>"
+    else:
+        kname = "alphabet_kernel<" + ("protein" if p["alphabet"] == "protein" else "triplet") + ",%s>"
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
     n_ins, n_q = ins.n_records, qry.n_records
@@ -318,7 +376,10 @@ def main():
         N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
         N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), n_q, out.data_ptr(), sh)
 
-    rmw_ceiling = random_rmw_ceiling(torch) if args.workload.startswith("out-of-cache") else None
+    # the random-RMW ceiling (an 8 GiB probe) for filters larger than L2,
+    # except at the profiling sizes
+    rmw_ceiling = (random_rmw_ceiling(torch)
+                   if spec["bits"] > 8 * (129 << 20) and not args.workload.endswith("-small") else None)
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -350,7 +411,7 @@ def main():
         raise RuntimeError("device status error in the timed region")
 
     words = out.cpu().numpy().view(np.uint32)
-    fpr = fpr_of(words, qry)
+    fpr = fpr_of(words, qry, p["k"], B)
     value = throughput(world, args.steps, nk_ins + nk_q, total)
 
     # rooflines: insert against HBM (one 32-byte sector read and written per
@@ -358,7 +419,9 @@ def main():
     peaks, peak_src = measured_peaks()
     avg_ins, avg_q = s_ins / args.steps, s_q / args.steps
     sha = kernel_source_sha()
-    runs_i, runs_q = runs_estimate(ins), runs_estimate(qry)
+    runs_i = runs_estimate(ins, p["k"], p["m"], B)
+    runs_q = runs_estimate(qry, p["k"], p["m"], B)
+    ops = alu_ops(p)
     bytes_ins = ins.n_bases + 8 * (n_ins + 1) + 64 * runs_i
     bytes_q = qry.n_bases + 8 * (n_q + 1) + 32 * runs_q + 4 * ((qry.n_bases + 31) // 32)
 
@@ -369,7 +432,7 @@ def main():
         return None
 
     ins_ach = bytes_ins / avg_ins / 1e9
-    roof_ins = {"bound": "hbm", "kernel": "strip_kernel<31,16,28,4,insert>",
+    roof_ins = {"bound": "hbm", "kernel": kname % "insert",
                 "achieved": ins_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ins_ach / peaks["hbm_gbs"], "traffic": traffic_of("insert", nk_ins),
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
@@ -381,15 +444,15 @@ def main():
                     "torch index_add_) over an 8 GiB tensor, measured in this run",
             "rows_per_s": rmw_ceiling, "runs_per_s": runs_i / avg_ins,
             "frac": runs_i / avg_ins / rmw_ceiling}
-    q_ach = ALU_OPS_PER_KMER["query"] * nk_q / avg_q / 1e12
-    roof_q = {"bound": "alu", "kernel": "strip_kernel<31,16,28,4,query>",
+    q_ach = ops["query"] * nk_q / avg_q / 1e12
+    roof_q = {"bound": "alu", "kernel": kname % "query",
               "achieved": q_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (ALU pipe)",
               "frac": q_ach / ALU_PEAK_TOPS, "traffic": traffic_of("query", nk_q),
               "peak_source": "152 SMs x 64 ALU lanes x 2.07 GHz (recipe SM count and clock)",
-              "ops_per_kmer": ALU_OPS_PER_KMER["query"], "avg_launch_ms": 1e3 * avg_q,
+              "ops_per_kmer": ops["query"], "avg_launch_ms": 1e3 * avg_q,
               "algorithmic_bytes_per_kmer": bytes_q / nk_q,
               "hbm_frac": bytes_q / avg_q / 1e9 / peaks["hbm_gbs"]}
-    ins_alu = ALU_OPS_PER_KMER["insert"] * nk_ins / avg_ins / 1e12
+    ins_alu = ops["insert"] * nk_ins / avg_ins / 1e12
     roof_ins["alu_frac"] = ins_alu / ALU_PEAK_TOPS
     roofline, roofline_other = (roof_ins, roof_q) if avg_ins >= avg_q else (roof_q, roof_ins)
 
@@ -399,20 +462,23 @@ def main():
 
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(ins, qry, spec["bits"])
+        cb = cpu_baseline(ins, qry, spec["bits"], p=p)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "k-mers/s", "n_gpus": world,
+            "metric": metric_of(p), "value": value, "unit": "k-mers/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64 (integer)",
             "data": "synthetic",
-            "config": {"workload": spec["desc"], "k": K, "m": M, "s": S, "H": H, "seed": SEED,
+            "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
+                       "alphabet": p["alphabet"], "seed": SEED,
                        "filter_bits": spec["bits"], "insert_kmers": nk_ins, "query_kmers": nk_q,
                        "insert_records": n_ins, "query_records": n_q,
-                       "l2": "inputs larger than L2 (sequences 1 GB each, filter 8 GiB)"
-                             if args.workload == "out-of-cache" else "see workload",
+                       "l2": {"out-of-cache": "inputs larger than L2 (sequences 1 GB each, filter 8 GiB)",
+                              "protein-like": "inputs larger than L2 (sequences 0.5 GB each, filter 1 GiB)",
+                              "triplet": "inputs larger than L2 (sequences 1 GB each, filter 1 GiB)"}
+                             .get(args.workload, "see workload"),
                        "filter_between_steps": "not cleared (insert is idempotent; same work)",
                        "replicas": world},
             "insert_kmers_per_s": throughput(world, args.steps, nk_ins, s_ins),
@@ -420,7 +486,7 @@ def main():
             "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
             "roofline": roofline, "roofline_other_kernel": roofline_other,
             "gpu_launches": 4 * args.steps,
-            "gpu_launches_note": "per step: offsets check + strip kernel for insert and for query",
+            "gpu_launches_note": "per step: offsets check + insert kernel, offsets check + query kernel",
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cb,
             "wall_s_timed": t_wall,
         }
@@ -468,8 +534,9 @@ def _timed(torch, fn, warmup=2, reps=3):
 
 
 def run_suite(args):
-    """One JSON line per configuration (tiny, genome-like, irregular) and per
-    point of the (s, m, H) sweep at k = 31 and 2^30 bits: insert and query
+    """One JSON line per configuration (tiny, genome-like, irregular, the
+    protein-like and triplet alphabets) and per point of the (s, m, H) sweep at
+    k = 31 and 2^30 bits: insert and query
     k-mers/s (CUDA events, device-resident inputs) and the false-positive
     rate.  Parity of every point is covered by the tests."""
     import torch
@@ -481,8 +548,12 @@ def run_suite(args):
     def dev(wl):
         return torch.from_numpy(wl.seq).cuda(), torch.from_numpy(wl.offsets).cuda()
 
-    def measure(name, ins, qry, bits, k=K, m=M, s=S, H=H, fpr_qry=None, extra=None):
-        sbf = SuperBloomFilter(bits, k=k, m=m, s=s, H=H, seed=SEED)
+    def measure(name, ins, qry, bits, k=K, m=M, s=S, H=H, fpr_qry=None, extra=None, p=None):
+        alphabet = "dna"
+        if p is not None:
+            k, m, s, H, alphabet = p["k"], p["m"], p["s"], p["H"], p["alphabet"]
+        B = 3 if alphabet == "dna_triplet" else 1
+        sbf = SuperBloomFilter(bits, k=k, m=m, s=s, H=H, seed=SEED, alphabet=alphabet)
         di, dio = dev(ins)
         dq, dqo = dev(qry)
         out = torch.zeros((qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
@@ -515,12 +586,12 @@ def run_suite(args):
             fpr, n_fpr = positives / max(n_valid, 1), n_valid
             del ones
         else:
-            fpr, n_fpr = fpr_of(words, fq, k), fpr_count(fq, k)
-        line = {"suite": name, "k": k, "m": m, "s": s, "H": H, "filter_bits": bits,
-                "specialized": sbf.specialized, "insert_kmers": kmer_count(ins, k),
-                "query_kmers": kmer_count(qry, k),
-                "insert_kmers_per_s": kmer_count(ins, k) / t_ins,
-                "query_kmers_per_s": kmer_count(qry, k) / t_q, "fpr": fpr,
+            fpr, n_fpr = fpr_of(words, fq, k, B), fpr_count(fq, k, B)
+        line = {"suite": name, "alphabet": alphabet, "k": k, "m": m, "s": s, "H": H,
+                "filter_bits": bits, "specialized": sbf.specialized,
+                "insert_kmers": kmer_count(ins, k, B), "query_kmers": kmer_count(qry, k, B),
+                "insert_kmers_per_s": kmer_count(ins, k, B) / t_ins,
+                "query_kmers_per_s": kmer_count(qry, k, B) / t_q, "fpr": fpr,
                 "fpr_kmers": n_fpr}
         line.update(extra or {})
         print(json.dumps(line), flush=True)
@@ -543,6 +614,12 @@ def run_suite(args):
     i_ins, i_qry = synth.irregular()
     i_qry.meta["is_random"] = np.ones(i_qry.n_records, dtype=bool)
     measure("irregular", i_ins, i_qry, 1 << 32)
+    del i_ins, i_qry
+    for name in ("protein-like", "triplet"):
+        spec = WORKLOADS[name]
+        a_ins, a_qry = spec["make"]()
+        measure(name, a_ins, a_qry, spec["bits"], p=spec["p"])
+        del a_ins, a_qry
 
 
 def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):

@@ -94,8 +94,10 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
  * width; hashing, sharding and bit addressing are those of sbf_create.  Insert
  * and query keep their contracts with "position" meaning a byte of the
  * concatenated input: the k-mer starting at a symbol's first byte g answers at
- * bit g, and (triplets) bits of other bytes are 0.  These filters always run
- * the runtime-parameter alphabet kernel (sbf_is_specialized returns 0).
+ * bit g, and (triplets) bits of other bytes are 0.  Protein (12, 8, 10, 4) and
+ * triplet (10, 5, 8, 4) have compile-time specialised kernels
+ * (sbf_is_specialized returns 1); every other valid (k, m, s, H) runs the
+ * runtime-parameter alphabet kernel with the same results.
  * Returns NULL on error, like sbf_create. */
 sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet);
 

@@ -1,8 +1,8 @@
 // sbf_alphabet.cu -- SBF insert/query kernels for the protein and DNA-triplet
 // alphabets ("cuSBF", Sec. IV-A: proteins, 26 symbols in 5 bits; DNA triplets,
-// 64 symbols in 6 bits, each symbol read from several input bytes).  Runtime
-// k, m, s, H with k * bits <= 64 (Sec. IV-C: one k-mer packs into one 64-bit
-// word, so protein k <= 12 and triplet k <= 10).
+// 64 symbols in 6 bits, each symbol read from several input bytes).  k * bits
+// <= 64 (Sec. IV-C: one k-mer packs into one 64-bit word, so protein k <= 12
+// and triplet k <= 10).
 //
 // Symbols.  Protein: the 26 letters, either case, A..Z = 0..25; every other
 // byte is invalid.  Triplet: a codon of three bases read in frame from the
@@ -15,23 +15,27 @@
 // Work layout (the paper's shared tile preparation, Sec. IV-C, with the
 // per-position hashes kept in shared memory instead of recomputed per
 // k-mer):
-//  * a block owns a tile of TB = 256*B consecutive bytes starting at a
-//    multiple of 32, and walks the tiles grid-stride;
-//  * warp 0 locates the record boundaries that fall in the tile (plus the
-//    k-mer overhang) and marks them in a bitmap; the other warps load the
-//    tile's bytes and turn them into symbol codes;
+//  * a block owns a contiguous range of tiles of TB = 256*B bytes (tile
+//    starts are multiples of 32); the record boundaries of a tile (plus the
+//    k-mer overhang) are loaded in one parallel round from the first boundary
+//    after the tile start, carried over from the previous tile, and marked in
+//    a bitmap; the tile's bytes become one symbol code per byte;
 //  * the tile is covered in B passes; in pass p lane t owns byte B*t + p, so
 //    within one record the lanes of a pass that start a symbol hold
 //    consecutive k-mers (for triplets, one pass of three carries each
 //    record's frame);
-//  * per pass, every position computes its m-mer hash and its s-mer's four
-//    word masks once (shared memory), then every k-mer takes the minimum over
-//    its w = k-m+1 m-mer hashes (Algorithm 1) and ORs its k-s+1 s-mer masks;
-//  * insert: lanes holding consecutive valid k-mers with one shard are
-//    merged by a segmented OR over the warp (the paper's super-k-mer runs,
-//    Fig. 3) and the head lane issues one atomicOr per non-zero word;
-//    query: each valid k-mer tests its shard's four words (Algorithm 2) and
-//    the answers are assembled in shared memory and stored coalesced.
+//  * per pass, every slot packs its symbols once and stores its m-mer hash and
+//    its s-mer's four word masks (shared memory); symbol validity is one
+//    ballot bit per slot.  Every k-mer then takes the minimum over its
+//    w = k-m+1 m-mer hashes (Algorithm 1);
+//  * insert: lanes holding consecutive valid k-mers with one shard form a run
+//    (the paper's super-k-mer runs, Fig. 3); the run's head lane ORs the s-mer
+//    masks of the run's contiguous s-mer slots and issues one atomicOr per
+//    non-zero word.  Query: each valid k-mer ORs its k-s+1 s-mer masks, tests
+//    its shard's four words (Algorithm 2) and the answers are assembled in
+//    shared memory and stored coalesced.
+// The benchmarked parameter points have compile-time specialisations; every
+// other valid (k, m, s, H) runs the same kernel with runtime loop bounds.
 #include "sbf_device.cuh"
 #include "sbf_kernels.h"
 
@@ -51,20 +55,23 @@ struct AlphaCfg<kAlphabetTriplet> {
 
 constexpr int kAlphaThreads = 256;
 constexpr uint32_t kBadCode = 0xFFu;
+constexpr int64_t kNoStart = INT64_MIN;
 
 template <int ALPHA>
 struct AlphaTile {
     static constexpr int B = AlphaCfg<ALPHA>::B, BITS = AlphaCfg<ALPHA>::BITS, KMAX = AlphaCfg<ALPHA>::KMAX;
     static constexpr int NT = kAlphaThreads;
-    static constexpr int TB = NT * B;                  // tile bytes (k-mer start positions)
-    static constexpr int CODES = TB + B * (KMAX - 1);  // symbol codes, one per start byte
-    static constexpr int RAW = CODES + B - 1;          // bytes the codes read
-    static constexpr int HN = NT + KMAX - 1;           // hash slots per pass
-    static constexpr int SPAN = TB + B * KMAX;         // boundary bitmap reach
-    static constexpr int BW = (SPAN + 31) / 32 + 1;    // bitmap words (+1: two-word reads)
-    static constexpr int OUTW = TB / 32;               // answer words per tile
+    static constexpr int TB = NT * B;                 // tile bytes (k-mer start positions)
+    static constexpr int HN = NT + KMAX - 1;          // hash slots per pass
+    static constexpr int CODES = TB + 2 * B * KMAX;   // symbol codes (one per start byte), padded
+    static constexpr int RAW = CODES + B - 1;         // bytes the codes read
+    static constexpr int SPAN = TB + B * KMAX;        // boundary bitmap reach
+    static constexpr int BW = (SPAN + 31) / 32 + 1;   // bitmap words (+1: two-word reads)
+    static constexpr int VW = (HN + 31) / 32 + 1;     // symbol-valid words per pass
+    static constexpr int OUTW = TB / 32;              // answer words per tile
     static_assert(TB % 32 == 0, "tiles must cover whole answer words");
     static_assert(B * KMAX - 1 < 32, "a k-mer's inner boundaries must fit one 32-bit window");
+    static_assert(KMAX - 1 <= 32, "halo slots are filled by warp 0");
 };
 
 template <int ALPHA>
@@ -73,14 +80,13 @@ struct AlphaSmem {
     uint64_t hm[T::HN];      // m-mer hash at slot u (byte B*u + pass)
     uint64_t sk[4][T::HN];   // s-mer word masks at slot u
     uint32_t starts[T::BW];  // bit i: a record boundary at byte t0 + i (i >= 1)
+    uint32_t symok[T::VW];   // bit u: the symbol at slot u is valid
     uint32_t ans[T::OUTW];
     int64_t prev_start;      // last boundary <= t0, or kNoStart
-    uint8_t mok[T::HN];      // m-mer at slot u is valid
+    int64_t r_start;         // first boundary index with offsets[r] > t0
     uint8_t raw[ALPHA == kAlphabetTriplet ? T::RAW : 1];
     uint8_t code[T::CODES];
 };
-
-constexpr int64_t kNoStart = INT64_MIN;
 
 __device__ __forceinline__ uint32_t protein_code(uint32_t c) {
     const uint32_t u = (c | 0x20u) - (uint32_t)'a';  // A..Z and a..z -> 0..25
@@ -92,11 +98,11 @@ __device__ __forceinline__ uint32_t codon_code(uint32_t c0, uint32_t c1, uint32_
     return (a | b | c) < 0 ? kBadCode : (uint32_t)(a * 16 + b * 4 + c);
 }
 
-// Any bit in [from, from + len) of the bitmap, 0 <= len <= 31.
-__device__ __forceinline__ bool any_bit(const uint32_t *bm, int from, int len) {
+// Bits [from, from + len) of a bitmap as the low bits of a word, 0 <= len <= 32.
+__device__ __forceinline__ uint32_t bits_at(const uint32_t *bm, int from, int len) {
     const int w = from >> 5;
     const uint64_t two = (uint64_t)bm[w] | ((uint64_t)bm[w + 1] << 32);
-    return ((two >> (from & 31)) & ((1ull << len) - 1ull)) != 0;
+    return (uint32_t)((two >> (from & 31)) & ((1ull << len) - 1ull));
 }
 
 // Highest boundary at or below tile byte j (absolute), else prev.
@@ -107,55 +113,86 @@ __device__ __forceinline__ int64_t start_at_or_below(const uint32_t *bm, int j, 
     return b ? t0 + 32 * w + 31 - __clz(b) : prev;
 }
 
-template <int ALPHA, bool kQuery>
+// The s-mer's H bits as four word masks; compile-time H when H_ > 0.
+template <int H_>
+__device__ __forceinline__ void smer_words(uint64_t hs, int H, uint64_t K[4]) {
+    K[0] = K[1] = K[2] = K[3] = 0ull;
+    if constexpr (H_ > 0) {
+        constexpr int SW = 64 / H_;
+#pragma unroll
+        for (int i = 0; i < H_; ++i) {
+            uint32_t pos;
+            if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
+            else pos = (uint32_t)((hs * salt_of(i)) >> 58);
+            K[i & 3] |= 1ull << pos;
+        }
+    } else {
+        smer_bits_runtime(hs, H, K);
+    }
+}
+
+// K_ > 0: compile-time (k, m, s, H); K_ == 0: the launch's runtime values.
+template <int ALPHA, int K_, int M_, int S_, int H_, bool kQuery>
 __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
     using T = AlphaTile<ALPHA>;
     constexpr int B = T::B, BITS = T::BITS, KMAX = T::KMAX, NT = T::NT, TB = T::TB;
+    constexpr bool kStatic = K_ > 0;
     __shared__ AlphaSmem<ALPHA> sm;
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
     const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
     if (hi <= lo) return;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int k = a.k, m = a.m, s = a.s, w = k - m + 1, z1 = k - s + 1;
+    const int k = kStatic ? K_ : a.k, m = kStatic ? M_ : a.m, s = kStatic ? S_ : a.s;
+    const int w = k - m + 1, z1 = k - s + 1, L = m > s ? m : s;
     const int kspan = B * k;
-    const uint64_t seed_s = ~a.seed;
-    const int n_words = a.H < 4 ? a.H : 4;
+    const uint64_t seed_m = a.seed, seed_s = ~a.seed;
+    const int n_words = kStatic ? (H_ < 4 ? H_ : 4) : (a.H < 4 ? a.H : 4);
     const int64_t base = lo & ~int64_t(31);
     const int64_t n_tiles = (hi - base + TB - 1) / TB;
+    // this block's contiguous tile range
+    const int64_t tile_b = n_tiles * blockIdx.x / gridDim.x;
+    const int64_t tile_e = n_tiles * (blockIdx.x + 1) / gridDim.x;
+    if (tile_b >= tile_e) return;
 
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    for (int i = t; i < T::BW; i += NT) sm.starts[i] = 0u;
+    if (kQuery)
+        for (int i = t; i < T::OUTW; i += NT) sm.ans[i] = 0u;
+    if (warp == 0) {
+        const int64_t r0 = warp_find_boundary(a.offsets, a.n, base + tile_b * TB, lo, hi, lane);
+        if (lane == 0) sm.r_start = r0;
+    }
+    __syncthreads();
+
+    for (int64_t tile = tile_b; tile < tile_e; ++tile) {
         const int64_t t0 = base + tile * TB;
-        // ---- record boundaries (warp 0) and symbol codes (warps 1..7)
-        for (int i = t; i < T::BW; i += NT) sm.starts[i] = 0u;
-        if (kQuery)
-            for (int i = t; i < T::OUTW; i += NT) sm.ans[i] = 0u;
-        __syncthreads();
-        if (warp == 0) {
-            const int64_t r0 = warp_find_boundary(a.offsets, a.n, t0, lo, hi, lane);
-            if (lane == 0) sm.prev_start = r0 >= 1 ? a.offsets[r0 - 1] : kNoStart;
-            const int64_t lim = t0 + T::SPAN;
-            // boundaries r0, r0+1, ... are > t0 and non-decreasing: stop once
-            // the warp's last one reaches lim (or runs past offsets[n])
-            for (int64_t rb = r0; rb <= a.n; rb += 32) {
-                const int64_t r = rb + lane;
-                const int64_t p = r <= a.n ? a.offsets[r] : lim;
-                if (p < lim) atomicOr(&sm.starts[(p - t0) >> 5], 1u << ((p - t0) & 31));
-                if (__shfl_sync(0xffffffffu, p, 31) >= lim) break;
+        const int64_t lim = t0 + T::SPAN;
+        // ---- record boundaries in (t0, lim), from r_start on, one round per NT
+        const int64_t r_start = sm.r_start;
+        if (t == 0) sm.prev_start = r_start >= 1 ? a.offsets[r_start - 1] : kNoStart;
+        int n_le = 0;  // boundaries <= t0 + TB (block-wide count)
+        for (int64_t rb = r_start;; rb += NT) {
+            const int64_t r = rb + t;
+            const int64_t p = r <= a.n ? a.offsets[r] : INT64_MAX;
+            // (p > t0 holds for every r >= r_start; checked so that the bitmap
+            // index stays in range whatever the offsets hold)
+            if (p > t0 && p < lim) atomicOr(&sm.starts[(p - t0) >> 5], 1u << ((p - t0) & 31));
+            n_le += __syncthreads_count(p <= t0 + TB);
+            if (!__syncthreads_or(t == NT - 1 && p < lim)) break;
+        }
+        // ---- symbol codes
+        if constexpr (B == 1) {
+            for (int u = t; u < T::CODES; u += NT) {
+                const int64_t g = t0 + u;
+                sm.code[u] = (uint8_t)(g >= lo && g < hi ? protein_code(a.seq[g]) : kBadCode);
             }
         } else {
-            if constexpr (B == 1) {
-                for (int u = t - 32; u < T::CODES; u += NT - 32) {
-                    const int64_t g = t0 + u;
-                    sm.code[u] = (uint8_t)(g >= lo && g < hi ? protein_code(a.seq[g]) : kBadCode);
-                }
-            } else {
-                for (int u = t - 32; u < T::RAW; u += NT - 32) {
-                    const int64_t g = t0 + u;
-                    sm.raw[u] = g >= lo && g < hi ? a.seq[g] : (uint8_t)0;
-                }
+            for (int u = t; u < T::RAW; u += NT) {
+                const int64_t g = t0 + u;
+                sm.raw[u] = g >= lo && g < hi ? a.seq[g] : (uint8_t)0;
             }
         }
         __syncthreads();
+        if (t == 0) sm.r_start = r_start + n_le;
         if constexpr (B > 1) {
             for (int u = t; u < T::CODES; u += NT)
                 sm.code[u] = (uint8_t)codon_code(sm.raw[u], sm.raw[u + 1], sm.raw[u + 2]);
@@ -174,72 +211,64 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
                 }
                 if (!__syncthreads_or(in_frame)) continue;
             }
-            const bool placed = in_frame && g + kspan <= hi && !any_bit(sm.starts, j + 1, kspan - 1);
+            const bool placed = in_frame && g + kspan <= hi && bits_at(sm.starts, j + 1, kspan - 1) == 0u;
 
-            // ---- per-slot hashes: slot u covers byte B*u + pass
+            // ---- per slot (byte B*u + pass): pack max(m, s) symbols once; the
+            //      m-mer and s-mer are its leading symbols.  Slots that are out
+            //      of frame are never read by a placed k-mer of this pass.
+            // (each code is cut to BITS bits: the invalid marker would
+            // otherwise spill into the field above it, and a symbol past the
+            // shorter of the two windows may be invalid in a valid k-mer)
             auto fill = [&](int u) {
                 const int pos = B * u + pass;
-                if (u < NT + w - 1) {
-                    uint64_t v = 0;
-                    uint32_t bad = 0;
+                uint64_t v = 0;
 #pragma unroll
-                    for (int i = 0; i < KMAX; ++i)
-                        if (i < m) {
-                            const uint32_t c = sm.code[pos + B * i];
-                            bad |= c;
-                            v = (v << BITS) | c;
-                        }
-                    sm.hm[u] = hash_minimizer(v, a.seed);
-                    sm.mok[u] = (uint8_t)((bad & 0x80u) == 0);
-                }
-                if (u < NT + z1 - 1) {
-                    uint64_t v = 0;
-                    uint32_t bad = 0;
+                for (int i = 0; i < L; ++i) v = (v << BITS) | (sm.code[pos + B * i] & ((1u << BITS) - 1u));
+                sm.hm[u] = hash_minimizer(v >> (BITS * (L - m)), seed_m);
+                uint64_t K[4];
+                smer_words<H_>(hash_smer(v >> (BITS * (L - s)), seed_s), a.H, K);
 #pragma unroll
-                    for (int i = 0; i < KMAX; ++i)
-                        if (i < s) {
-                            const uint32_t c = sm.code[pos + B * i];
-                            bad |= c;
-                            v = (v << BITS) | c;
-                        }
-                    uint64_t K[4] = {0, 0, 0, 0};
-                    smer_bits_runtime(hash_smer(v, seed_s), a.H, K);
-                    const bool ok = (bad & 0x80u) == 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) sm.sk[q][u] = ok ? K[q] : 0ull;
-                }
+                for (int q = 0; q < 4; ++q) sm.sk[q][u] = K[q];
             };
-            // an out-of-frame slot is never read by a placed k-mer of this pass
             if (B == 1 || in_frame) fill(t);
             if (t < KMAX - 1) fill(NT + t);
+            {
+                const unsigned ok = __ballot_sync(0xffffffffu, sm.code[j] != kBadCode);
+                if (lane == 0) sm.symok[warp] = ok;
+                if (warp == 0) {
+                    const unsigned okh =
+                        __ballot_sync(0xffffffffu, lane < KMAX - 1 && sm.code[B * (NT + lane) + pass] != kBadCode);
+                    if (lane == 0) sm.symok[NT / 32] = okh;
+                }
+            }
             __syncthreads();
 
             // ---- this lane's k-mer from the slots
-            bool valid = placed;
-            uint64_t shard = 0, K[4] = {0, 0, 0, 0};
-            if (placed) {
+            bool valid = placed && bits_at(sm.symok, t, k) == (uint32_t)((1ull << k) - 1ull);
+            uint64_t shard = 0;
+            if (valid) {
                 uint64_t mu = ~0ull;
 #pragma unroll
-                for (int i = 0; i < KMAX; ++i)
-                    if (i < w) {
-                        valid &= sm.mok[t + i] != 0;
-                        const uint64_t h = sm.hm[t + i];
-                        mu = h < mu ? h : mu;
-                    }
+                for (int i = 0; i < w; ++i) {
+                    const uint64_t h = sm.hm[t + i];
+                    mu = h < mu ? h : mu;
+                }
                 shard = mu & a.shard_mask;
-#pragma unroll
-                for (int i = 0; i < KMAX; ++i)
-                    if (i < z1) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) K[q] |= sm.sk[q][t + i];
-                    }
             }
             if (kQuery) {
                 bool present = false;
                 if (valid) {
+                    uint64_t K0 = 0, K1 = 0, K2 = 0, K3 = 0;
+#pragma unroll
+                    for (int i = 0; i < z1; ++i) {
+                        K0 |= sm.sk[0][t + i];
+                        K1 |= sm.sk[1][t + i];
+                        K2 |= sm.sk[2][t + i];
+                        K3 |= sm.sk[3][t + i];
+                    }
                     const ulonglong2 *F = reinterpret_cast<const ulonglong2 *>(a.words + shard * 4);
                     const ulonglong2 f01 = __ldg(F), f23 = __ldg(F + 1);
-                    present = ((K[0] & ~f01.x) | (K[1] & ~f01.y) | (K[2] & ~f23.x) | (K[3] & ~f23.y)) == 0;
+                    present = ((K0 & ~f01.x) | (K1 & ~f01.y) | (K2 & ~f23.x) | (K3 & ~f23.y)) == 0;
                 }
                 if constexpr (B == 1) {
                     const unsigned bits = __ballot_sync(0xffffffffu, present);
@@ -248,26 +277,28 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
                     if (present) atomicOr(&sm.ans[j >> 5], 1u << (j & 31));
                 }
             } else {
-                // runs of lanes with one shard: segmented OR toward the run head
+                // runs: consecutive lanes with one shard; the head lane ORs the
+                // run's s-mer slots [t, t + run length + k-s)
                 const uint64_t key = valid ? shard : (1ull << 63) | (uint64_t)lane;
                 const uint64_t prev_key = __shfl_up_sync(0xffffffffu, key, 1);
                 const bool head = lane == 0 || prev_key != key;
                 const unsigned heads = __ballot_sync(0xffffffffu, head);
                 const unsigned after = heads & ~((2u << lane) - 1u);
                 const int end = after ? __ffs(after) - 1 : 32;
-                if (__any_sync(0xffffffffu, end > lane + 1)) {
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint64_t v = __shfl_down_sync(0xffffffffu, K[q], d);
-                            if (lane + d < end) K[q] |= v;
-                        }
-                }
                 if (head && valid) {
+                    uint64_t K0 = 0, K1 = 0, K2 = 0, K3 = 0;
+                    const int last = t + (end - lane) + z1 - 1;
+                    for (int u = t; u < last; ++u) {
+                        K0 |= sm.sk[0][u];
+                        K1 |= sm.sk[1][u];
+                        K2 |= sm.sk[2][u];
+                        K3 |= sm.sk[3][u];
+                    }
                     unsigned long long *F = reinterpret_cast<unsigned long long *>(a.words + shard * 4);
-                    for (int q = 0; q < n_words; ++q)
-                        if (K[q]) atomicOr(F + q, K[q]);
+                    const uint64_t Kq[4] = {K0, K1, K2, K3};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < n_words && Kq[q]) atomicOr(F + q, Kq[q]);
                 }
             }
             __syncthreads();
@@ -281,21 +312,53 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
             }
         }
         __syncthreads();
+        for (int i = t; i < T::BW; i += NT) sm.starts[i] = 0u;
+        if (kQuery)
+            for (int i = t; i < T::OUTW; i += NT) sm.ans[i] = 0u;
+        __syncthreads();
     }
+}
+
+struct AlphaEntry {
+    int alphabet, k, m, s, H;
+    const void *insert, *query;
+};
+
+template <int ALPHA, int K, int M, int S, int H>
+constexpr AlphaEntry alpha_entry() {
+    return AlphaEntry{ALPHA, K, M, S, H, reinterpret_cast<const void *>(&alphabet_kernel<ALPHA, K, M, S, H, false>),
+                      reinterpret_cast<const void *>(&alphabet_kernel<ALPHA, K, M, S, H, true>)};
 }
 
 }  // namespace
 
-const void *alphabet_insert_kernel(int alphabet) {
-    if (alphabet == kAlphabetProtein) return reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetProtein, false>);
-    if (alphabet == kAlphabetTriplet) return reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetTriplet, false>);
-    return nullptr;
-}
-
-const void *alphabet_query_kernel(int alphabet) {
-    if (alphabet == kAlphabetProtein) return reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetProtein, true>);
-    if (alphabet == kAlphabetTriplet) return reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetTriplet, true>);
-    return nullptr;
+bool find_alphabet_kernels(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
+                           bool *specialized) {
+    // the benchmarked points (protein 12/8/10/4, triplet 10/5/8/4), then the
+    // runtime-parameter kernels
+    static const AlphaEntry table[] = {
+        alpha_entry<kAlphabetProtein, 12, 8, 10, 4>(),
+        alpha_entry<kAlphabetTriplet, 10, 5, 8, 4>(),
+    };
+    for (const AlphaEntry &e : table)
+        if (e.alphabet == alphabet && e.k == k && e.m == m && e.s == s && e.H == H) {
+            *insert = e.insert;
+            *query = e.query;
+            *specialized = true;
+            return true;
+        }
+    *specialized = false;
+    if (alphabet == kAlphabetProtein) {
+        *insert = reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetProtein, 0, 0, 0, 0, false>);
+        *query = reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetProtein, 0, 0, 0, 0, true>);
+        return true;
+    }
+    if (alphabet == kAlphabetTriplet) {
+        *insert = reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetTriplet, 0, 0, 0, 0, false>);
+        *query = reinterpret_cast<const void *>(&alphabet_kernel<kAlphabetTriplet, 0, 0, 0, 0, true>);
+        return true;
+    }
+    return false;
 }
 
 }  // namespace sbf

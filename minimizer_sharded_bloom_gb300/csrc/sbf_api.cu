@@ -237,8 +237,9 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     int threads = 0;
     // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
     if (alphabet != SBF_ALPHABET_DNA) {
-        ins = sbf::alphabet_insert_kernel(alphabet);
-        qry = sbf::alphabet_query_kernel(alphabet);
+        bool spec = false;
+        sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec);
+        f->specialized = spec;
         threads = 256;
     } else if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;

@@ -12,10 +12,12 @@ const void *generic_insert_kernel();
 const void *generic_query_kernel();
 __global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status);
 
-// Protein and DNA-triplet kernels (runtime k, m, s, H), sbf_alphabet.cu;
-// nullptr for any other alphabet.  256 threads per block.
-const void *alphabet_insert_kernel(int alphabet);
-const void *alphabet_query_kernel(int alphabet);
+// Protein and DNA-triplet kernels, sbf_alphabet.cu: the compile-time
+// specialisation for (k, m, s, H) when there is one (*specialized = true),
+// else the runtime-parameter kernel.  False for any other alphabet.  256
+// threads per block.
+bool find_alphabet_kernels(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
+                           bool *specialized);
 
 // Compile-time specialised kernels.  Returns false when (k, m, s, H) has no
 // specialisation; *insert / *query / *threads are set otherwise.

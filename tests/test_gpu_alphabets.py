@@ -12,8 +12,13 @@ from _gpu_helpers import (assert_images_equal, assert_words_equal, gpu_insert, g
 
 pytestmark = pytest.mark.gpu
 
-PROTEIN = dict(k=12, m=6, s=10, H=4)
+# the compile-time specialised points (the benchmark's parameters)
+PROTEIN = dict(k=12, m=8, s=10, H=4)
 TRIPLET = dict(k=10, m=5, s=8, H=4)
+
+
+def _specialized(alphabet, params):
+    return params == (PROTEIN if alphabet == "protein" else TRIPLET)
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +29,7 @@ def torch():
 def _filter(num_bits, params, seed, alphabet):
     from minimizer_sharded_bloom_gb300 import SuperBloomFilter
     f = SuperBloomFilter(num_bits, seed=seed, alphabet=alphabet, **params)
-    assert not f.specialized
+    assert f.specialized == _specialized(alphabet, params)
     return f
 
 
@@ -74,10 +79,13 @@ def test_mixed_records_random_params(torch, alphabet, case):
                pad_front=case % 2 * 5)
 
 
-@pytest.mark.parametrize("alphabet,params", [("protein", PROTEIN), ("dna_triplet", TRIPLET)])
+@pytest.mark.parametrize("alphabet,params", [
+    ("protein", PROTEIN), ("dna_triplet", TRIPLET),
+    ("protein", dict(k=12, m=6, s=10, H=4)), ("dna_triplet", dict(k=10, m=6, s=8, H=4))])
 def test_benchmark_params_long_records(torch, alphabet, params):
-    """The benchmark's parameters on long records (many tiles per record,
-    frame kept across tiles) and offsets[0] > 0, not a multiple of 32."""
+    """The benchmark's parameters (compile-time kernels) and neighbours of
+    them (runtime kernels) on long records (many tiles per record, frame kept
+    across tiles) and offsets[0] > 0, not a multiple of 32."""
     rng = np.random.default_rng(71)
     body = _records(rng, alphabet, 7, 20_000, 60_000, 1)
     lead = 77
@@ -120,7 +128,8 @@ def test_edge_cases(torch, alphabet):
     tiny = _records(rng, alphabet, 5000, 1, 4, 0)
     cases.append(tiny)
     for p in (dict(k=1, m=1, s=1, H=1), dict(k=kmax, m=kmax, s=kmax, H=32),
-              dict(k=kmax, m=1, s=1, H=7)):
+              dict(k=kmax, m=1, s=1, H=7), dict(k=kmax, m=2, s=kmax - 1, H=5),
+              PROTEIN if alphabet == "protein" else TRIPLET):
         for wl in cases:
             _roundtrip(torch, alphabet, wl, wl, p, 1 << 10, seed=9)
     assert N.sbf_get_alphabet(_filter(1 << 10, dict(k=3, m=2, s=2, H=2), 1, alphabet).handle) == \
