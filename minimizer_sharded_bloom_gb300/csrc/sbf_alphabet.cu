@@ -74,7 +74,7 @@ struct AlphaTile {
     static_assert(KMAX - 1 <= 32, "halo slots are filled by warp 0");
 };
 
-template <int ALPHA>
+template <int ALPHA, bool kQuery>
 struct AlphaSmem {
     using T = AlphaTile<ALPHA>;
     uint64_t hm[T::HN];      // m-mer hash at slot u (byte B*u + pass)
@@ -82,6 +82,7 @@ struct AlphaSmem {
     uint32_t starts[T::BW];  // bit i: a record boundary at byte t0 + i (i >= 1)
     uint32_t symok[T::VW];   // bit u: the symbol at slot u is valid
     uint32_t ans[T::OUTW];
+    uint32_t racc[8][kQuery ? 1 : T::NT];  // insert: run masks (word halves) by head thread
     int64_t prev_start;      // last boundary <= t0, or kNoStart
     int64_t r_start;         // first boundary index with offsets[r] > t0
     uint8_t raw[ALPHA == kAlphabetTriplet ? T::RAW : 1];
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
     using T = AlphaTile<ALPHA>;
     constexpr int B = T::B, BITS = T::BITS, KMAX = T::KMAX, NT = T::NT, TB = T::TB;
     constexpr bool kStatic = K_ > 0;
-    __shared__ AlphaSmem<ALPHA> sm;
+    __shared__ AlphaSmem<ALPHA, kQuery> sm;
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
     const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
     if (hi <= lo) return;
@@ -154,6 +155,26 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
     const int64_t tile_e = n_tiles * (blockIdx.x + 1) / gridDim.x;
     if (tile_b >= tile_e) return;
 
+    // A tile's inputs are loaded one tile ahead into registers (raw bytes, 0
+    // outside [lo, hi); the first NT record boundaries from the tile's first
+    // boundary index on; the boundary before it) and stored to shared memory
+    // after the previous tile's passes, so their latency overlaps compute.
+    constexpr int NBYTES = (B == 1) ? T::CODES : T::RAW;
+    constexpr int NPF = (NBYTES + NT - 1) / NT;
+    uint32_t pf_byte[NPF];
+    int64_t pf_bound = INT64_MAX, pf_prev = kNoStart;
+    auto prefetch = [&](int64_t t0n, int64_t r_from) {
+#pragma unroll
+        for (int i = 0; i < NPF; ++i) {
+            const int u = t + i * NT;
+            const int64_t g = t0n + u;
+            pf_byte[i] = (u < NBYTES && g >= lo && g < hi) ? (uint32_t)a.seq[g] : 0u;
+        }
+        const int64_t r = r_from + t;
+        pf_bound = r <= a.n ? a.offsets[r] : INT64_MAX;
+        if (t == 0) pf_prev = r_from >= 1 ? a.offsets[r_from - 1] : kNoStart;
+    };
+
     for (int i = t; i < T::BW; i += NT) sm.starts[i] = 0u;
     if (kQuery)
         for (int i = t; i < T::OUTW; i += NT) sm.ans[i] = 0u;
@@ -162,37 +183,41 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
         if (lane == 0) sm.r_start = r0;
     }
     __syncthreads();
+    int64_t r_cur = sm.r_start;  // first boundary index with offsets[r] > t0 (block-uniform)
+    prefetch(base + tile_b * TB, r_cur);
 
     for (int64_t tile = tile_b; tile < tile_e; ++tile) {
         const int64_t t0 = base + tile * TB;
         const int64_t lim = t0 + T::SPAN;
-        // ---- record boundaries in (t0, lim), from r_start on, one round per NT
-        const int64_t r_start = sm.r_start;
-        if (t == 0) sm.prev_start = r_start >= 1 ? a.offsets[r_start - 1] : kNoStart;
+        // ---- record boundaries in (t0, lim): the prefetched round, then more
+        //      rounds of NT while the last one is still inside
+        if (t == 0) sm.prev_start = pf_prev;
         int n_le = 0;  // boundaries <= t0 + TB (block-wide count)
-        for (int64_t rb = r_start;; rb += NT) {
-            const int64_t r = rb + t;
-            const int64_t p = r <= a.n ? a.offsets[r] : INT64_MAX;
-            // (p > t0 holds for every r >= r_start; checked so that the bitmap
-            // index stays in range whatever the offsets hold)
-            if (p > t0 && p < lim) atomicOr(&sm.starts[(p - t0) >> 5], 1u << ((p - t0) & 31));
-            n_le += __syncthreads_count(p <= t0 + TB);
-            if (!__syncthreads_or(t == NT - 1 && p < lim)) break;
-        }
-        // ---- symbol codes
-        if constexpr (B == 1) {
-            for (int u = t; u < T::CODES; u += NT) {
-                const int64_t g = t0 + u;
-                sm.code[u] = (uint8_t)(g >= lo && g < hi ? protein_code(a.seq[g]) : kBadCode);
+        {
+            int64_t p = pf_bound;
+            for (int64_t rb = r_cur;;) {
+                // (p > t0 holds for every r >= r_cur; checked so that the
+                // bitmap index stays in range whatever the offsets hold)
+                if (p > t0 && p < lim) atomicOr(&sm.starts[(p - t0) >> 5], 1u << ((p - t0) & 31));
+                n_le += __syncthreads_count(p <= t0 + TB);
+                if (!__syncthreads_or(t == NT - 1 && p < lim)) break;
+                rb += NT;
+                const int64_t r = rb + t;
+                p = r <= a.n ? a.offsets[r] : INT64_MAX;
             }
-        } else {
-            for (int u = t; u < T::RAW; u += NT) {
-                const int64_t g = t0 + u;
-                sm.raw[u] = g >= lo && g < hi ? a.seq[g] : (uint8_t)0;
+        }
+        // ---- symbol codes (protein) or raw bytes (triplets)
+#pragma unroll
+        for (int i = 0; i < NPF; ++i) {
+            const int u = t + i * NT;
+            if (u < NBYTES) {
+                if constexpr (B == 1) sm.code[u] = (uint8_t)protein_code(pf_byte[i]);
+                else sm.raw[u] = (uint8_t)pf_byte[i];
             }
         }
         __syncthreads();
-        if (t == 0) sm.r_start = r_start + n_le;
+        r_cur += n_le;
+        if (tile + 1 < tile_e) prefetch(t0 + TB, r_cur);
         if constexpr (B > 1) {
             for (int u = t; u < T::CODES; u += NT)
                 sm.code[u] = (uint8_t)codon_code(sm.raw[u], sm.raw[u + 1], sm.raw[u + 2]);
@@ -255,7 +280,7 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
                 }
                 shard = mu & a.shard_mask;
             }
-            if (kQuery) {
+            if constexpr (kQuery) {
                 bool present = false;
                 if (valid) {
                     uint64_t K0 = 0, K1 = 0, K2 = 0, K3 = 0;
@@ -277,25 +302,50 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
                     if (present) atomicOr(&sm.ans[j >> 5], 1u << (j & 31));
                 }
             } else {
-                // runs: consecutive lanes with one shard; the head lane ORs the
-                // run's s-mer slots [t, t + run length + k-s)
+                // this k-mer's mask, then runs: consecutive lanes with one shard.
+                // Lanes after a run's head OR their masks into the head's column
+                // of `racc` (32-bit shared atomics); the head then issues one
+                // atomicOr per non-zero word.
+                uint64_t Kq[4] = {0, 0, 0, 0};
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < z1; ++i) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) Kq[q] |= sm.sk[q][t + i];
+                    }
+                }
                 const uint64_t key = valid ? shard : (1ull << 63) | (uint64_t)lane;
                 const uint64_t prev_key = __shfl_up_sync(0xffffffffu, key, 1);
                 const bool head = lane == 0 || prev_key != key;
                 const unsigned heads = __ballot_sync(0xffffffffu, head);
-                const unsigned after = heads & ~((2u << lane) - 1u);
-                const int end = after ? __ffs(after) - 1 : 32;
-                if (head && valid) {
-                    uint64_t K0 = 0, K1 = 0, K2 = 0, K3 = 0;
-                    const int last = t + (end - lane) + z1 - 1;
-                    for (int u = t; u < last; ++u) {
-                        K0 |= sm.sk[0][u];
-                        K1 |= sm.sk[1][u];
-                        K2 |= sm.sk[2][u];
-                        K3 |= sm.sk[3][u];
+                const int head_lane = 31 - __clz(heads & (0xFFFFFFFFu >> (31 - lane)));
+                if (__any_sync(0xffffffffu, head_lane != lane)) {
+                    if (head) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            sm.racc[2 * q][t] = (uint32_t)Kq[q];
+                            sm.racc[2 * q + 1][t] = (uint32_t)(Kq[q] >> 32);
+                        }
                     }
+                    __syncwarp();
+                    if (!head && valid) {
+                        const int col = (t & ~31) + head_lane;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (q < n_words) {
+                                atomicOr(&sm.racc[2 * q][col], (uint32_t)Kq[q]);
+                                atomicOr(&sm.racc[2 * q + 1][col], (uint32_t)(Kq[q] >> 32));
+                            }
+                    }
+                    __syncwarp();
+                    if (head) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            Kq[q] = (uint64_t)sm.racc[2 * q][t] | ((uint64_t)sm.racc[2 * q + 1][t] << 32);
+                    }
+                }
+                if (head && valid) {
                     unsigned long long *F = reinterpret_cast<unsigned long long *>(a.words + shard * 4);
-                    const uint64_t Kq[4] = {K0, K1, K2, K3};
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         if (q < n_words && Kq[q]) atomicOr(F + q, Kq[q]);

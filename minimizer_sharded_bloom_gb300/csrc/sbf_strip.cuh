@@ -230,6 +230,7 @@ struct StripSmem {
     uint32_t starts[C::BIT_WORDS];      // record-start bit per code index
     uint32_t valid[C::TILE_WORDS + 2];  // validity bit per k-mer of the tile
     uint32_t outw[C::TILE_WORDS + 2];   // query answer bits of the tile
+    uint2 onehot[64];                   // halves of 1 << p, p = 0 .. 63
     uint64_t raw_bar;                                   // completes the raw bulk copy
     int abort_flag;
     alignas(16) unsigned char raw[C::RAW_BYTES];        // the tile's sequence bytes (bulk copy)
@@ -237,8 +238,12 @@ struct StripSmem {
 
 
 // The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1).
-template <int H>
-__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8]) {
+// kTable: the one-hot halves of a bit position come from a 64-entry shared
+// table (tab[p] = halves of 1 << p), one shared load instead of a variable
+// 64-bit shift on the ALU pipe (the query, ALU-bound, gains ~4 %; the insert
+// does not).
+template <int H, bool kTable>
+__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab) {
     constexpr int SW = 64 / H;
 #pragma unroll
     for (int j = 0; j < 8; ++j) m[j] = 0u;
@@ -247,9 +252,15 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8]) {
         uint32_t pos;
         if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
         else pos = (uint32_t)((hs * salt_of(i)) >> 58);
-        const uint64_t one = 1ull << pos;
-        m[2 * (i & 3)] |= (uint32_t)one;
-        m[2 * (i & 3) + 1] |= (uint32_t)(one >> 32);
+        if constexpr (kTable) {
+            const uint2 one = tab[pos];
+            m[2 * (i & 3)] |= one.x;
+            m[2 * (i & 3) + 1] |= one.y;
+        } else {
+            const uint64_t one = 1ull << pos;
+            m[2 * (i & 3)] |= (uint32_t)one;
+            m[2 * (i & 3) + 1] |= (uint32_t)(one >> 32);
+        }
     }
 }
 
@@ -284,6 +295,8 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
         mbar_init(&sm.raw_bar, 1);
         sm.abort_flag = 0;
     }
+    if (kQuery && tid < 64)
+        sm.onehot[tid] = make_uint2(tid < 32 ? 1u << tid : 0u, tid >= 32 ? 1u << (tid - 32) : 0u);
     __syncthreads();
     uint32_t raw_phase = 0;
     if (tid == 0 && blockIdx.x < n_tiles && bulk_ok(blockIdx.x))
@@ -396,7 +409,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                 codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
                 for (int z = 0; z < Z; ++z)
-                    smer_halves<H>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1]);
+                    smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mk[0][j] = 0u;
             }
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                         for (int z = 0; z < Z; ++z)
 #pragma unroll
                             for (int j = 0; j < 8; ++j) mk[z][j] = mk[z + 1][j];
-                        smer_halves<H>(hash_smer(win_value(wv, i, S), seed_s), mk[Z]);
+                        smer_halves<H, kQuery>(hash_smer(win_value(wv, i, S), seed_s), mk[Z], sm.onehot);
                         // OR of the k-mer's older s-mers (its newest is mk[Z])
                         uint32_t older[8];
 #pragma unroll
