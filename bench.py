@@ -125,14 +125,20 @@ def alu_ops(p):
 ALU_PEAK_TOPS = 152 * 64 * 2.07e9 / 1e12
 
 # ncu DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per k-mer of
-# the out-of-cache launches (profiles/strip_kernel_out_of_cache.md), valid only
-# for the kernel source they were measured on.
-MEASURED_TRAFFIC = {"source_sha": "264a4f79d9f6da28", "insert": 14.4131, "query": 20.6667}
+# the full-size launches of each workload (summaries under profiles/), valid
+# only for the kernel source they were measured on.
+MEASURED_TRAFFIC = {
+    "out-of-cache": {"source_sha": "4c315582d62385e5", "insert": 14.4167, "query": 20.7774},
+    "protein-like": {"source_sha": "79ade69e6c6d6309", "insert": 36.1087, "query": 43.0310},
+    "triplet": {"source_sha": "79ade69e6c6d6309", "insert": 32.9667, "query": 40.3148},
+}
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(p=MAIN) -> str:
+    """Hash of the source files the workload's kernels are built from."""
+    files = ("sbf_strip.cuh", "sbf_device.cuh") if p["alphabet"] == "dna" else ("sbf_alphabet.cu", "sbf_device.cuh")
     h = hashlib.sha256()
-    for name in ("sbf_strip.cuh", "sbf_device.cuh"):
+    for name in files:
         with open(os.path.join(ROOT, "minimizer_sharded_bloom_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -418,7 +424,7 @@ def main():
     # run), query against the ALU pipe; "roofline" is the dominant (longer) one.
     peaks, peak_src = measured_peaks()
     avg_ins, avg_q = s_ins / args.steps, s_q / args.steps
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(p)
     runs_i = runs_estimate(ins, p["k"], p["m"], B)
     runs_q = runs_estimate(qry, p["k"], p["m"], B)
     ops = alu_ops(p)
@@ -426,9 +432,9 @@ def main():
     bytes_q = qry.n_bases + 8 * (n_q + 1) + 32 * runs_q + 4 * ((qry.n_bases + 31) // 32)
 
     def traffic_of(name, nk):
-        if (MEASURED_TRAFFIC["source_sha"] == sha and MEASURED_TRAFFIC[name] is not None
-                and args.workload == "out-of-cache"):
-            return MEASURED_TRAFFIC[name] * nk
+        rec = MEASURED_TRAFFIC.get(args.workload)
+        if rec and rec["source_sha"] == sha and rec[name] is not None:
+            return rec[name] * nk
         return None
 
     ins_ach = bytes_ins / avg_ins / 1e9
