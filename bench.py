@@ -331,6 +331,10 @@ def main():
     ap.add_argument("--workload", default="out-of-cache", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--host-mode", type=int, default=None, choices=[0, 1],
+                    help="e2e leg: 0 reads host buffers in place, 1 stages chunks (default: the library's)")
+    ap.add_argument("--host-chunk", type=int, default=None,
+                    help="e2e leg: positions per staged chunk (default: the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="measure every configuration and the sweep grid (one JSON line each)")
@@ -464,6 +468,10 @@ def main():
 
     e2e = None
     if not args.no_e2e:
+        if args.host_mode is not None:
+            N.sbf_set_host_mode(sbf.handle, args.host_mode)
+        if args.host_chunk is not None:
+            N.sbf_set_host_chunk(sbf.handle, args.host_chunk)
         e2e = run_e2e(torch, N, sbf, ins, qry, nk_ins + nk_q, pg, world, min(args.steps, 3))
 
     cb = None

@@ -148,10 +148,17 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         return set_error(SBF_ERR_INVALID_ARG, "host call: bad arguments");
     if (n == 0) return SBF_OK;
     if (off[0] < 0) return set_error(SBF_ERR_BAD_OFFSETS, "offsets[0] < 0");
-    for (int64_t r = 0; r < n; ++r)
-        if (off[r + 1] < off[r]) return set_error(SBF_ERR_BAD_OFFSETS, "offsets decrease at record %lld", (long long)r);
+    // The whole-array check runs on the host only where the host needs valid
+    // offsets (an empty range, the staged path's chunking); in place, the
+    // device check kernel covers them and sbf_get_status reports them.
+    auto host_check = [&]() -> int {
+        for (int64_t r = 0; r < n; ++r)
+            if (off[r + 1] < off[r])
+                return set_error(SBF_ERR_BAD_OFFSETS, "offsets decrease at record %lld", (long long)r);
+        return SBF_OK;
+    };
     const int64_t lo = off[0], hi = off[n];
-    if (hi <= lo) return SBF_OK;
+    if (hi <= lo) return host_check();
     const int seq_kind = host_kind(seq + lo);
     const int out_kind = query ? host_kind(out_bits + (lo >> 5)) : 0;
     if (seq_kind < 0 || out_kind < 0 || host_kind(off) < 0)
@@ -163,6 +170,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         int rc = SBF_OK;
         if (run_in_place(f, seq, off, n, out_bits, user_stream, query, &rc)) return rc;
     }
+    if (int rc = host_check()) return rc;
     if (!f->stager) f->stager = new Stager;
     Stager &st = *static_cast<Stager *>(f->stager);
 

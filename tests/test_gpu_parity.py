@@ -180,6 +180,35 @@ def test_bad_offsets_set_the_status(torch):
     assert_images_equal(sbf.to_numpy(), oracle_image(seq, good, MAIN, 1 << 14, 4))
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_host_calls_report_bad_offsets(torch, mode):
+    """Host-facing insert/query with decreasing offsets fail with
+    SBF_ERR_BAD_OFFSETS (found by the device check when the buffers are read
+    in place, mode 0; by the host before chunking, mode 1), change nothing,
+    leave the status clear, and the next good call works."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(14)
+    seq = synth.uniform_bases(rng, 4000)
+    good = np.array([0, 2000, 4000], dtype=np.int64)
+    bad = np.array([0, 3000, 2000, 4000], dtype=np.int64)
+    sbf = _filter(1 << 14, MAIN, 4)
+    N.sbf_set_host_mode(sbf.handle, mode)
+    with pytest.raises(N.SBFError) as err:
+        sbf.insert_host(seq, bad)
+    assert err.value.code == N.SBF_ERR_BAD_OFFSETS
+    assert not sbf.to_numpy().any()
+    assert sbf.status() == 0
+    out = np.full(4000 // 32 + 2, 0xDEADBEEF, dtype=np.uint32)
+    with pytest.raises(N.SBFError) as err:
+        sbf.query_host(seq, bad, out=out)
+    assert err.value.code == N.SBF_ERR_BAD_OFFSETS
+    assert sbf.status() == 0
+    sbf.insert_host(seq, good)
+    F = oracle_image(seq, good, MAIN, 1 << 14, 4)
+    assert_images_equal(sbf.to_numpy(), F)
+    assert_words_equal(sbf.query_host(seq, good), oracle_answers(F, seq, good, MAIN, 4), good)
+
+
 def test_filter_algebra_on_gpu(torch):
     """Order independence, split inserts, idempotence and union, on the GPU
     image (OR is commutative and idempotent)."""
