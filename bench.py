@@ -136,7 +136,8 @@ MEASURED_TRAFFIC = {
 
 def kernel_source_sha(p=MAIN) -> str:
     """Hash of the source files the workload's kernels are built from."""
-    files = ("sbf_strip.cuh", "sbf_device.cuh") if p["alphabet"] == "dna" else ("sbf_alphabet.cu", "sbf_device.cuh")
+    files = {"dna": ("sbf_strip.cuh", "sbf_device.cuh"), "protein": ("sbf_strip.cuh", "sbf_device.cuh"),
+             "dna_triplet": ("sbf_alphabet.cu", "sbf_device.cuh")}[p["alphabet"]]
     h = hashlib.sha256()
     for name in files:
         with open(os.path.join(ROOT, "minimizer_sharded_bloom_gb300", "csrc", name), "rb") as f:
@@ -376,8 +377,11 @@ def main():
         raise RuntimeError("the benchmark configuration must run its specialised kernel")
     if p["alphabet"] == "dna":
         kname = f"strip_kernel<{p['k']},{p['m']},{p['s']},{p['H']},%s>"
+    elif p["alphabet"] == "protein" and sbf.specialized:
+        kname = f"strip_kernel<{p['k']},{p['m']},{p['s']},{p['H']},%s,protein>"
     else:
-        kname = "alphabet_kernel<" + ("protein" if p["alphabet"] == "protein" else "triplet") + ",%s>"
+        kname = (f"alphabet_kernel<{'protein' if p['alphabet'] == 'protein' else 'triplet'},"
+                 f"{p['k']},{p['m']},{p['s']},{p['H']},%s>")
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
     n_ins, n_q = ins.n_records, qry.n_records
@@ -388,7 +392,8 @@ def main():
 
     # the random-RMW ceiling (an 8 GiB probe) for filters larger than L2,
     # except at the profiling sizes
-    rmw_ceiling = (random_rmw_ceiling(torch)
+    rmw_gib = max(1, spec["bits"] >> 33)  # the probe spans the filter's size
+    rmw_ceiling = (random_rmw_ceiling(torch, gib=rmw_gib)
                    if spec["bits"] > 8 * (129 << 20) and not args.workload.endswith("-small") else None)
     for _ in range(max(args.warmup, 0)):
         step()
@@ -451,7 +456,7 @@ def main():
     if rmw_ceiling:
         roof_ins["pattern_peak"] = {
             "what": "random 32-byte row read-modify-write (4 x 64-bit atomic add per row, "
-                    "torch index_add_) over an 8 GiB tensor, measured in this run",
+                    f"torch index_add_) over a {rmw_gib} GiB tensor (the filter's size), measured in this run",
             "rows_per_s": rmw_ceiling, "runs_per_s": runs_i / avg_ins,
             "frac": runs_i / avg_ins / rmw_ceiling}
     q_ach = ops["query"] * nk_q / avg_q / 1e12

@@ -89,11 +89,6 @@ struct AlphaSmem {
     uint8_t code[T::CODES];
 };
 
-__device__ __forceinline__ uint32_t protein_code(uint32_t c) {
-    const uint32_t u = (c | 0x20u) - (uint32_t)'a';  // A..Z and a..z -> 0..25
-    return u < 26u ? u : kBadCode;
-}
-
 __device__ __forceinline__ uint32_t codon_code(uint32_t c0, uint32_t c1, uint32_t c2) {
     const int a = base_code(c0), b = base_code(c1), c = base_code(c2);
     return (a | b | c) < 0 ? kBadCode : (uint32_t)(a * 16 + b * 4 + c);

@@ -24,6 +24,8 @@ extern const StripEntry kStripEntriesMain[];
 extern const int kStripCountMain;
 extern const StripEntry kStripEntriesLargeH[];
 extern const int kStripCountLargeH;
+extern const StripEntry kStripEntriesProtein[];
+extern const int kStripCountProtein;
 #ifdef SBF_WITH_SWEEP
 #define SBF_DECLARE_UNIT(M, S)                       \
     extern const StripEntry kStripEntriesM##M##S##_[]; \
@@ -31,6 +33,19 @@ extern const int kStripCountLargeH;
 SBF_SWEEP_UNITS(SBF_DECLARE_UNIT)
 #undef SBF_DECLARE_UNIT
 #endif
+
+bool find_protein_strip(int k, int m, int s, int H, const void **insert, const void **query, int *threads) {
+    for (int i = 0; i < kStripCountProtein; ++i) {
+        const StripEntry &e = kStripEntriesProtein[i];
+        if (e.k == k && e.m == m && e.s == s && e.H == H) {
+            *insert = e.insert;
+            *query = e.query;
+            *threads = e.threads;
+            return true;
+        }
+    }
+    return false;
+}
 
 bool find_specialized(int k, int m, int s, int H, const void **insert, const void **query,
                       int *threads) {
@@ -236,7 +251,10 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     const void *ins = nullptr, *qry = nullptr;
     int threads = 0;
     // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
-    if (alphabet != SBF_ALPHABET_DNA) {
+    if (alphabet == SBF_ALPHABET_PROTEIN && shards <= (1ull << 31) &&
+        sbf::find_protein_strip(k, m, s, H, &ins, &qry, &threads)) {
+        f->specialized = true;
+    } else if (alphabet != SBF_ALPHABET_DNA) {
         bool spec = false;
         sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec);
         f->specialized = spec;

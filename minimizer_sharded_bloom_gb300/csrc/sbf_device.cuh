@@ -58,6 +58,13 @@ __device__ __forceinline__ int base_code(uint32_t c) {
     return ok ? code : -1;
 }
 
+// Protein symbol code of one byte (Sec. IV-A: 26 letters, 5 bits): A..Z and
+// a..z -> 0..25; any other byte -> a value >= 26 (0xFF).
+__device__ __forceinline__ uint32_t protein_code(uint32_t c) {
+    const uint32_t u = (c | 0x20u) - (uint32_t)'a';
+    return u < 26u ? u : 0xFFu;
+}
+
 // Salt of hash index i for H > 10 (Sec. IV-G: "per-hash-index golden-ratio-
 // derived salt"): output i of SplitMix64 from state 0, whose state advances by
 // the golden-ratio constant, made odd.

@@ -39,6 +39,14 @@
 // Shared-memory indexing: code index ci <-> absolute base position
 // T0 - 16 + ci, where T0 (a multiple of 32) is the tile's first k-mer; the
 // k-mer at T0 + kk therefore starts at code index kk + 16.
+//
+// Alphabets (Sec. IV-A): A = 0 is DNA as above.  A = 1 is the protein
+// alphabet (26 letters, 5 bits per symbol, one byte per symbol): the front end
+// stores one 5-bit code per byte instead of the 2-bit words, and pass A / pass
+// B roll their m-mer / s-mer values forward by one symbol per position
+// (v = v << 5 | code) instead of cutting them out of 64-base windows.  Validity,
+// record starts, the sliding minimum, runs and the query's shard slots are the
+// same code.
 #pragma once
 
 #include <cstdint>
@@ -61,6 +69,47 @@ __device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
     for (int wd = 0; wd < 4; ++wd) {
         if (wd >= H) continue;
         asm volatile("red.global.or.b64 [%0], %1;" ::"l"(F + wd), "l"(v[wd]) : "memory");
+    }
+}
+
+// Cooperative flush over the warp's active lanes `am`: the runs that end at
+// this step (`flush` set, the run's shard in `key`, its masks in `acc`) are
+// reduced as (run, word) pairs spread over the active lanes, pair 4r + w to
+// the lane of rank (4r + w) mod n_active, so a run's four words leave in one
+// instruction (when four or more lanes are active) and reach L2 as one
+// 32-byte sector request instead of four.  The loop's trip count,
+// ceil(4 * runs / n_active) <= 128, is the same on every lane.
+template <int H>
+__device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const uint32_t acc[8], bool flush,
+                                           unsigned am) {
+    const unsigned fm = __ballot_sync(am, flush);
+    if (!fm) return;
+    const int lane = threadIdx.x & 31;
+    const int rank = __popc(am & ((1u << lane) - 1u));
+    const int n_act = __popc(am);
+    const int pairs = 4 * __popc(fm);
+    for (int base = 0; base < pairs; base += n_act) {
+        const int pidx = base + rank;
+        const int rr = pidx >> 2, wd = pidx & 3;
+        // source lane: the rr-th (from 0) set bit of fm, clearing at most 31 bits
+        unsigned m = fm;
+        for (int j = 0; j < rr && j < 31; ++j) m &= m - 1u;
+        const int src = (pidx < pairs && m) ? __ffs(m) - 1 : __ffs(fm) - 1;
+        const uint32_t k = __shfl_sync(am, key, src);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t l = __shfl_sync(am, acc[2 * q], src);
+            const uint32_t h = __shfl_sync(am, acc[2 * q + 1], src);
+            if (wd == q) {
+                lo = l;
+                hi = h;
+            }
+        }
+        if (pidx < pairs && wd < H && (lo | hi)) {
+            const uint64_t v = ((uint64_t)hi << 32) | lo;
+            asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)k * 4 + wd), "l"(v) : "memory");
+        }
     }
 }
 
@@ -124,6 +173,25 @@ __device__ __forceinline__ uint64_t bits64_at(const uint32_t *bm, int bit) {
     const uint32_t lo = __funnelshift_r(a, b, sh);
     const uint32_t hi = __funnelshift_r(b, c, sh);
     return ((uint64_t)hi << 32) | lo;
+}
+
+// 16 bytes (w[0] holds bytes 0..3, little-endian) -> 16 protein codes, one
+// per byte in the same order (`out`), and `bad` with bit i set iff byte i is
+// not a letter.  An invalid byte gets code 31: every code fits 5 bits, so a
+// rolling shift never carries into the next symbol's field.
+__device__ __forceinline__ void encode16_protein(const uint32_t w[4], uint32_t out[4], uint32_t &bad) {
+    bad = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t o = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t c = protein_code((w[q] >> (8 * b)) & 0xFFu);
+            bad |= (uint32_t)(c >= 26u) << (4 * q + b);
+            o |= (c & 31u) << (8 * b);
+        }
+        out[q] = o;
+    }
 }
 
 // 64 bases starting at code index ci, as four words w[0..3] (first base in
@@ -203,12 +271,14 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int K_, int M_, int S_, int H_>
+template <int K_, int M_, int S_, int H_, int A_ = 0>
 struct StripCfg {
-    static constexpr int K = K_, M = M_, S = S_, H = H_;
+    static constexpr int K = K_, M = M_, S = S_, H = H_, A = A_;
+    static constexpr int BITS = A == 0 ? 2 : 5;         // bits per symbol
     static constexpr int W = K - M + 1;                 // m-mer windows per k-mer; block length
     static constexpr int Z = K - S;                     // s-mers per k-mer minus one
-    static constexpr int NB = (W >= 16) ? 8 : (128 + W - 1) / W;  // blocks per strip
+    // blocks per strip (protein: ~110 k-mers, so that four query CTAs fit an SM)
+    static constexpr int NB = A != 0 ? (110 + W - 1) / W : (W >= 16) ? 8 : (128 + W - 1) / W;
     static constexpr int L = NB * W;                    // k-mers per thread
     static constexpr int NT = 128;                      // threads per CTA
     static constexpr int TILE = NT * L;                 // k-mer positions per tile (multiple of 32)
@@ -216,16 +286,17 @@ struct StripCfg {
     static constexpr int CODE_WORDS = (TILE + K + 96) / 16 + 4;  // 16 bases per word
     static constexpr int BIT_WORDS = (CODE_WORDS + 1) / 2 + 2;   // one bit per code index
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
-    static constexpr int SLOTS = 6;                     // query: staged shards per thread per block
+    static constexpr int SLOTS = A == 0 ? 6 : 4;        // query: staged shards per thread per block
     static constexpr int RAW_BYTES = 16 * CODE_WORDS;   // a tile's bytes, staged by one bulk copy
     static_assert(W >= 1 && W <= 32 && Z >= 0 && H >= 1 && H <= kMaxH, "parameters");
+    static_assert(A == 0 || BITS * K <= 64, "a k-mer packs into one 64-bit word");
     static_assert(TILE % 32 == 0, "tile must cover whole output words");
 };
 
-template <int K, int M, int S, int H>
+template <int K, int M, int S, int H, int A = 0>
 struct StripSmem {
-    using C = StripCfg<K, M, S, H>;
-    uint32_t codes[C::CODE_WORDS];
+    using C = StripCfg<K, M, S, H, A>;
+    uint32_t codes[A == 0 ? C::CODE_WORDS : 1];  // DNA: 16 2-bit codes per word
     uint16_t bad16[2 * C::BIT_WORDS];   // bit per code index; read as uint32 words
     uint32_t starts[C::BIT_WORDS];      // record-start bit per code index
     uint32_t valid[C::TILE_WORDS + 2];  // validity bit per k-mer of the tile
@@ -234,6 +305,7 @@ struct StripSmem {
     uint64_t raw_bar;                                   // completes the raw bulk copy
     int abort_flag;
     alignas(16) unsigned char raw[C::RAW_BYTES];        // the tile's sequence bytes (bulk copy)
+    alignas(16) uint8_t pcode[A == 0 ? 16 : C::RAW_BYTES];  // protein: one 5-bit code per byte
 };
 
 
@@ -264,12 +336,14 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const ui
     }
 }
 
-template <int K, int M, int S, int H, bool kQuery>
-__global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchArgs a) {
-    using C = StripCfg<K, M, S, H>;
+template <int K, int M, int S, int H, bool kQuery, int A = 0>
+__global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(LaunchArgs a) {
+    using C = StripCfg<K, M, S, H, A>;
     constexpr int W = C::W, Z = C::Z, NB = C::NB, L = C::L, NT = C::NT, TILE = C::TILE;
-    constexpr int R = C::SLOTS;
-    __shared__ StripSmem<K, M, S, H> sm;
+    constexpr int R = C::SLOTS, BITS = C::BITS;
+    constexpr uint64_t kMaskM = A == 0 ? 0ull : (1ull << (BITS * M)) - 1ull;
+    constexpr uint64_t kMaskS = A == 0 ? 0ull : (1ull << (BITS * S)) - 1ull;
+    __shared__ StripSmem<K, M, S, H, A> sm;
     // query: shards of the current block's run heads, [slot][half][thread]
     __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
 
@@ -340,9 +414,16 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                 for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(sm.raw + 16 * c);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t code, bad;
-                    encode16(w, code, bad);
-                    sm.codes[c] = code;
+                    uint32_t bad;
+                    if constexpr (A == 0) {
+                        uint32_t code;
+                        encode16(w, code, bad);
+                        sm.codes[c] = code;
+                    } else {
+                        uint32_t o[4];
+                        encode16_protein(w, o, bad);
+                        *reinterpret_cast<uint4 *>(sm.pcode + 16 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
                     sm.bad16[c] = (uint16_t)bad;
                 }
             } else {
@@ -365,9 +446,16 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                             w[q] = x;
                         }
                     }
-                    uint32_t code, bad;
-                    encode16(w, code, bad);
-                    sm.codes[c] = code;
+                    uint32_t bad;
+                    if constexpr (A == 0) {
+                        uint32_t code;
+                        encode16(w, code, bad);
+                        sm.codes[c] = code;
+                    } else {
+                        uint32_t o[4];
+                        encode16_protein(w, o, bad);
+                        *reinterpret_cast<uint4 *>(sm.pcode + 16 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
                     sm.bad16[c] = (uint16_t)bad;
                 }
             }
@@ -393,6 +481,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
         // ---- phase 4: strips
         const int kk0 = tid * L;  // first k-mer of this thread (tile relative)
         if (T0 + kk0 < hi) {
+            const unsigned am = __activemask();  // the lanes that own a strip in this tile
             // m-mer u of the strip starts at code index kk0 + 15 + u; the strip's
             // k-mers are u = 1 .. L (k-mer kk0 + u - 1 starts at code index kk0 + 16 + u - 1).
             uint64_t suf[W];
@@ -403,13 +492,27 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                 suf[i] = ~0ull;
                 shard[i] = 0u;
             }
-            // the first Z s-mers of the strip's first k-mer
+            // the first Z s-mers of the strip's first k-mer.  Protein: vb rolls
+            // the s-mers (the last s symbols appended), va the m-mers.
+            uint64_t va = 0, vb = 0;
             {
-                uint32_t wv[4];
-                codes64_at(sm.codes, kk0 + 16, wv);
+                if constexpr (A == 0) {
+                    uint32_t wv[4];
+                    codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
-                for (int z = 0; z < Z; ++z)
-                    smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
+                    for (int z = 0; z < Z; ++z)
+                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < S - 1; ++i) vb = (vb << BITS) | sm.pcode[kk0 + 16 + i];
+#pragma unroll
+                    for (int z = 0; z < Z; ++z) {
+                        vb = (vb << BITS) | sm.pcode[kk0 + 16 + z + S - 1];
+                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot);
+                    }
+#pragma unroll
+                    for (int i = 0; i < M - 1; ++i) va = (va << BITS) | sm.pcode[kk0 + 15 + i];
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) mk[0][j] = 0u;
             }
@@ -438,12 +541,19 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                 if (blk > 0) vwin = bits64_at(sm.valid, kb);
                 {
                     uint32_t wv[4];
-                    codes64_at(sm.codes, kk0 + 15 + blk * W, wv);
+                    if constexpr (A == 0) codes64_at(sm.codes, kk0 + 15 + blk * W, wv);
                     uint64_t h[W];
                     uint64_t pre = ~0ull;
 #pragma unroll
                     for (int i = 0; i < W; ++i) {
-                        h[i] = hash_minimizer(win_value(wv, i, M), seed_m);
+                        uint64_t mv;
+                        if constexpr (A == 0) {
+                            mv = win_value(wv, i, M);
+                        } else {
+                            va = (va << BITS) | sm.pcode[kk0 + 15 + blk * W + i + M - 1];
+                            mv = va & kMaskM;
+                        }
+                        h[i] = hash_minimizer(mv, seed_m);
                         pre = h[i] < pre ? h[i] : pre;
                         if (i < W - 1) {
                             const uint64_t mu = suf[i + 1] < pre ? suf[i + 1] : pre;
@@ -487,7 +597,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                 //    code index kk + 16 + Z.
                 {
                     uint32_t wv[4];
-                    codes64_at(sm.codes, kb + 16 + Z, wv);
+                    if constexpr (A == 0) codes64_at(sm.codes, kb + 16 + Z, wv);
                     uint32_t present = 0;
                     int nb = 0;
                     if (kQuery) cp_async_wait<1>();
@@ -497,7 +607,14 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                         for (int z = 0; z < Z; ++z)
 #pragma unroll
                             for (int j = 0; j < 8; ++j) mk[z][j] = mk[z + 1][j];
-                        smer_halves<H, kQuery>(hash_smer(win_value(wv, i, S), seed_s), mk[Z], sm.onehot);
+                        uint64_t sv;
+                        if constexpr (A == 0) {
+                            sv = win_value(wv, i, S);
+                        } else {
+                            vb = (vb << BITS) | sm.pcode[kb + 16 + Z + i + S - 1];
+                            sv = vb & kMaskS;
+                        }
+                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot);
                         // OR of the k-mer's older s-mers (its newest is mk[Z])
                         uint32_t older[8];
 #pragma unroll
@@ -509,7 +626,13 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                         }
                         if (!kQuery) {
                             const uint32_t key = shard[i] | ((((uint32_t)(vwin >> i)) & 1u) ^ 1u) << 31;
-                            if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                            // DNA (runs of ~(w+1)/2 = 8.5 k-mers): each lane flushes its own
+                            // runs; protein (runs of ~3): the warp flushes cooperatively
+                            if constexpr (A == 0) {
+                                if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                            } else {
+                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am);
+                            }
                             const uint32_t same = key == cur_key ? 1u : 0u;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) acc[j] = keep_if(acc[j], same) | older[j] | mk[Z][j];
@@ -545,7 +668,13 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H>::NT) strip_kernel(LaunchA
                     }
                 }
             }
-            if (!kQuery && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+            if constexpr (!kQuery) {
+                if constexpr (A == 0) {
+                    if (!(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                } else {
+                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am);
+                }
+            }
         }
         __syncthreads();
         if (kQuery) {
@@ -567,11 +696,11 @@ struct StripEntry {
     int threads;
 };
 
-template <int K, int M, int S, int H>
+template <int K, int M, int S, int H, int A = 0>
 inline StripEntry strip_entry() {
-    return StripEntry{K, M, S, H, reinterpret_cast<const void *>(&strip_kernel<K, M, S, H, false>),
-                      reinterpret_cast<const void *>(&strip_kernel<K, M, S, H, true>),
-                      StripCfg<K, M, S, H>::NT};
+    return StripEntry{K, M, S, H, reinterpret_cast<const void *>(&strip_kernel<K, M, S, H, false, A>),
+                      reinterpret_cast<const void *>(&strip_kernel<K, M, S, H, true, A>),
+                      StripCfg<K, M, S, H, A>::NT};
 }
 
 }  // namespace sbf

@@ -99,6 +99,21 @@ def test_benchmark_params_long_records(torch, alphabet, params):
     assert np.array_equal(answer_bits(got, own), answer_bits(want, own))
 
 
+@pytest.mark.parametrize("case", range(6))
+def test_protein_strip_kernel_mixed(torch, case):
+    """The protein point runs the strip kernel (5-bit codes rolled per
+    position, cooperative run flushes): dirty ragged records (invalid bytes,
+    lowercase, empty and 1-byte records) over tens of tiles, on aligned
+    (bulk-copied tiles) and unaligned (direct loads) sequence pointers, and
+    shard counts from 1 to 2^20."""
+    rng = np.random.default_rng(7500 + case)
+    ins = _records(rng, "protein", int(rng.integers(20, 400)), 0, int(rng.integers(50, 4000)), 1 + case % 2)
+    qry = _with_own(ins, _records(rng, "protein", 300, 0, 300, 1))
+    num_bits = [256, 1 << 12, 1 << 16, 1 << 20, 1 << 24, 1 << 28][case]
+    _roundtrip(torch, "protein", ins, qry, PROTEIN, num_bits, seed=int(rng.integers(0, 2**62)),
+               pad_front=3 * (case % 2))
+
+
 @pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
 def test_edge_cases(torch, alphabet):
     """n = 0 (no work, output untouched); only empty records; records shorter
