@@ -11,6 +11,9 @@ bench.py times (the same library entry points and filter sizes).
   negatives), and (c) sampled answer bits of the full query equal the
   oracle's answers computed against the same image.
 * sweep: grid points at the full 50 Mbp against the oracle's whole image.
+* protein-like (5 x 10^8 residues, 2^33 bits; 10^7 fragments) and triplet
+  (the out-of-cache data as codons, 2^33 bits): (a)-(c) as for out-of-cache,
+  at the alphabets' benchmark parameters.
 """
 import numpy as np
 import pytest
@@ -29,9 +32,9 @@ def torch():
     return need_gpu()
 
 
-def _filter(num_bits, params, seed):
+def _filter(num_bits, params, seed, alphabet="dna"):
     from minimizer_sharded_bloom_gb300 import SuperBloomFilter
-    return SuperBloomFilter(num_bits, seed=seed, **params)
+    return SuperBloomFilter(num_bits, seed=seed, alphabet=alphabet, **params)
 
 
 def _gpu_words(torch, sbf, dseq, doff, total):
@@ -51,23 +54,24 @@ def _shard_rows(torch, sbf):
     return img, rows
 
 
-def _sparse_compare(torch, sbf, seq, offsets, params, seed):
+def _sparse_compare(torch, sbf, seq, offsets, params, seed, alphabet="dna"):
     """GPU image == oracle image, comparing only the oracle's non-zero shards
     plus a count of the GPU's non-zero shards."""
     img, rows = _shard_rows(torch, sbf)
     sh, words = oracle.insert_sparse(seq, offsets, params["k"], params["m"], params["s"],
-                                     params["H"], sbf.num_shards, seed)
+                                     params["H"], sbf.num_shards, seed, alphabet)
     nz = int((img != 0).any(dim=1).sum().item())
     assert nz == sh.size, (nz, sh.size)
     assert np.array_equal(rows(sh), words)
 
 
-def _sampled_checks(torch, sbf, ins, qry, params, seed, rng, n_samples=100_000):
+def _sampled_checks(torch, sbf, ins, qry, params, seed, rng, n_samples=100_000, alphabet="dna"):
     img, rows = _shard_rows(torch, sbf)
     # (b) no false negatives on sampled inserted k-mers, exact bits present
     pos = rng.integers(int(ins.offsets[0]), int(ins.offsets[-1]), size=n_samples)
     valid, shard, K = oracle.kmer_batch(ins.seq, ins.offsets, pos, params["k"], params["m"],
-                                        params["s"], params["H"], sbf.num_shards, seed)
+                                        params["s"], params["H"], sbf.num_shards, seed, alphabet)
+    assert valid.sum() > n_samples // 4
     F = rows(shard[valid])
     assert ((K[valid] & ~F) == 0).all()
     # (c) sampled answers of the full query
@@ -75,7 +79,7 @@ def _sampled_checks(torch, sbf, ins, qry, params, seed, rng, n_samples=100_000):
     words = _gpu_words(torch, sbf, dseq, doff, int(qry.offsets[-1]))
     qpos = rng.integers(int(qry.offsets[0]), int(qry.offsets[-1]), size=n_samples)
     want = oracle.query_sampled(rows, qry.seq, qry.offsets, qpos, params["k"], params["m"],
-                                params["s"], params["H"], sbf.num_shards, seed)
+                                params["s"], params["H"], sbf.num_shards, seed, alphabet)
     assert np.array_equal(answer_bits(words, qpos), want)
     return words
 
@@ -164,3 +168,36 @@ def test_irregular_full(torch):
     torch.cuda.synchronize()
     del dseq, doff
     _sampled_checks(torch, sbf, ins, qry, MAIN, seed, rng)
+
+
+@pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
+def test_alphabet_workload_full(torch, alphabet):
+    """The protein-like and triplet bench workloads at full size, with the
+    bench's filter size and parameters (protein runs the strip kernel)."""
+    if alphabet == "protein":
+        ins, qry = synth.protein_like()
+        params, seed = dict(k=12, m=8, s=10, H=4), 10
+    else:
+        ins, qry = synth.out_of_cache()
+        params, seed = dict(k=10, m=5, s=8, H=4), 11
+    rng = np.random.default_rng(99)
+    sub = _prefix(ins, 3_000_000)
+    sbf = _filter(1 << 33, params, seed, alphabet)
+    assert sbf.specialized
+    dseq, doff = to_dev(torch, sub.seq, sub.offsets)
+    sbf.insert(dseq, doff)
+    torch.cuda.synchronize()
+    _sparse_compare(torch, sbf, sub.seq, sub.offsets, params, seed, alphabet)
+    sbf.clear()
+    dseq, doff = to_dev(torch, ins.seq, ins.offsets)
+    sbf.insert(dseq, doff)
+    torch.cuda.synchronize()
+    del dseq, doff
+    assert sbf.status() == 0
+    words = _sampled_checks(torch, sbf, ins, qry, params, seed, rng, alphabet=alphabet)
+    # uniform fragments / reads: the false-positive rate stays small
+    B = 3 if alphabet == "dna_triplet" else 1
+    flen = int(np.diff(qry.offsets)[0])
+    starts = qry.offsets[:-1][qry.meta["is_random"]][:20000]
+    pos = (starts[:, None] + B * np.arange(flen // B - params["k"] + 1)[None, :]).reshape(-1)
+    assert answer_bits(words, pos).mean() < 0.01
