@@ -137,7 +137,7 @@ MEASURED_TRAFFIC = {
 def kernel_source_sha(p=MAIN) -> str:
     """Hash of the source files the workload's kernels are built from."""
     files = {"dna": ("sbf_strip.cuh", "sbf_device.cuh"), "protein": ("sbf_strip.cuh", "sbf_device.cuh"),
-             "dna_triplet": ("sbf_alphabet.cu", "sbf_device.cuh")}[p["alphabet"]]
+             "dna_triplet": ("sbf_strip.cuh", "sbf_alphabet.cu", "sbf_device.cuh")}[p["alphabet"]]
     h = hashlib.sha256()
     for name in files:
         with open(os.path.join(ROOT, "minimizer_sharded_bloom_gb300", "csrc", name), "rb") as f:
@@ -375,13 +375,18 @@ def main():
                            alphabet=p["alphabet"])
     if p["alphabet"] == "dna" and not sbf.specialized:
         raise RuntimeError("the benchmark configuration must run its specialised kernel")
-    if p["alphabet"] == "dna":
-        kname = f"strip_kernel<{p['k']},{p['m']},{p['s']},{p['H']},%s>"
-    elif p["alphabet"] == "protein" and sbf.specialized:
-        kname = f"strip_kernel<{p['k']},{p['m']},{p['s']},{p['H']},%s,protein>"
-    else:
-        kname = (f"alphabet_kernel<{'protein' if p['alphabet'] == 'protein' else 'triplet'},"
-                 f"{p['k']},{p['m']},{p['s']},{p['H']},%s>")
+    # which kernel runs each call: DNA and the protein point on the strip
+    # kernel; the triplet point inserts on the strip kernel and queries on the
+    # tiled alphabet kernel
+    pt = f"{p['k']},{p['m']},{p['s']},{p['H']}"
+    an = "protein" if p["alphabet"] == "protein" else "triplet"
+
+    def kname(kind):
+        if p["alphabet"] == "dna":
+            return f"strip_kernel<{pt},{kind}>"
+        if sbf.specialized and (p["alphabet"] == "protein" or kind == "insert"):
+            return f"strip_kernel<{pt},{kind},{an}>"
+        return f"alphabet_kernel<{an},{pt},{kind}>"
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
     n_ins, n_q = ins.n_records, qry.n_records
@@ -447,7 +452,7 @@ def main():
         return None
 
     ins_ach = bytes_ins / avg_ins / 1e9
-    roof_ins = {"bound": "hbm", "kernel": kname % "insert",
+    roof_ins = {"bound": "hbm", "kernel": kname("insert"),
                 "achieved": ins_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ins_ach / peaks["hbm_gbs"], "traffic": traffic_of("insert", nk_ins),
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
@@ -460,7 +465,7 @@ def main():
             "rows_per_s": rmw_ceiling, "runs_per_s": runs_i / avg_ins,
             "frac": runs_i / avg_ins / rmw_ceiling}
     q_ach = ops["query"] * nk_q / avg_q / 1e12
-    roof_q = {"bound": "alu", "kernel": kname % "query",
+    roof_q = {"bound": "alu", "kernel": kname("query"),
               "achieved": q_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (ALU pipe)",
               "frac": q_ach / ALU_PEAK_TOPS, "traffic": traffic_of("query", nk_q),
               "peak_source": "152 SMs x 64 ALU lanes x 2.07 GHz (recipe SM count and clock)",

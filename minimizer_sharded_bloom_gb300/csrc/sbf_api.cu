@@ -26,6 +26,8 @@ extern const StripEntry kStripEntriesLargeH[];
 extern const int kStripCountLargeH;
 extern const StripEntry kStripEntriesProtein[];
 extern const int kStripCountProtein;
+extern const StripEntry kStripEntriesTriplet[];
+extern const int kStripCountTriplet;
 #ifdef SBF_WITH_SWEEP
 #define SBF_DECLARE_UNIT(M, S)                       \
     extern const StripEntry kStripEntriesM##M##S##_[]; \
@@ -34,9 +36,13 @@ SBF_SWEEP_UNITS(SBF_DECLARE_UNIT)
 #undef SBF_DECLARE_UNIT
 #endif
 
-bool find_protein_strip(int k, int m, int s, int H, const void **insert, const void **query, int *threads) {
-    for (int i = 0; i < kStripCountProtein; ++i) {
-        const StripEntry &e = kStripEntriesProtein[i];
+bool find_alphabet_strip(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
+                         int *threads) {
+    const StripEntry *table = alphabet == SBF_ALPHABET_PROTEIN ? kStripEntriesProtein : kStripEntriesTriplet;
+    const int count = alphabet == SBF_ALPHABET_PROTEIN ? kStripCountProtein
+                      : alphabet == SBF_ALPHABET_DNA_TRIPLET ? kStripCountTriplet : 0;
+    for (int i = 0; i < count; ++i) {
+        const StripEntry &e = table[i];
         if (e.k == k && e.m == m && e.s == s && e.H == H) {
             *insert = e.insert;
             *query = e.query;
@@ -176,7 +182,7 @@ int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offse
     if (n == 0) return SBF_OK;
     cudaStream_t st = as_stream(stream);
     if (int rc = launch_check(f, offsets, n, st)) return rc;
-    return launch(f->query_kernel, f->grid_query, f->threads,
+    return launch(f->query_kernel, f->grid_query, f->threads_query,
                   make_args(f, seq, offsets, n, out_bits, device_seq), st);
 }
 
@@ -251,9 +257,20 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     const void *ins = nullptr, *qry = nullptr;
     int threads = 0;
     // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
-    if (alphabet == SBF_ALPHABET_PROTEIN && shards <= (1ull << 31) &&
-        sbf::find_protein_strip(k, m, s, H, &ins, &qry, &threads)) {
+    int threads_query = 0;
+    if (alphabet != SBF_ALPHABET_DNA && shards <= (1ull << 31) &&
+        sbf::find_alphabet_strip(alphabet, k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
+        threads_query = threads;
+        if (alphabet == SBF_ALPHABET_DNA_TRIPLET) {
+            // triplet queries of read batches mix the three frames inside every
+            // warp, so the strip kernel's frame passes cannot skip work there:
+            // the query keeps the tiled alphabet kernel
+            const void *unused = nullptr;
+            bool spec = false;
+            sbf::find_alphabet_kernels(alphabet, k, m, s, H, &unused, &qry, &spec);
+            threads_query = 256;
+        }
     } else if (alphabet != SBF_ALPHABET_DNA) {
         bool spec = false;
         sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec);
@@ -266,11 +283,13 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
         qry = sbf::generic_query_kernel();
         threads = 256;
     }
+    if (threads_query == 0) threads_query = threads;
     f->insert_kernel = ins;
     f->query_kernel = qry;
     f->threads = threads;
+    f->threads_query = threads_query;
     f->grid_insert = grid_for(ins, threads, sms);
-    f->grid_query = grid_for(qry, threads, sms);
+    f->grid_query = grid_for(qry, threads_query, sms);
     f->grid_check = 4 * sms;
     return f;
 }

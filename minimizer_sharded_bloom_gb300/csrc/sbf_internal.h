@@ -15,7 +15,8 @@ struct sbf_filter {
     int *status = nullptr;      // sticky device status
     const void *insert_kernel = nullptr;
     const void *query_kernel = nullptr;
-    int threads = 256;
+    int threads = 256;          // threads per block of the insert kernel
+    int threads_query = 256;    // ... and of the query kernel
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
     bool specialized = false;

@@ -12,9 +12,10 @@ const void *generic_insert_kernel();
 const void *generic_query_kernel();
 __global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status);
 
-// The protein alphabet's strip-kernel specialisations (shards <= 2^31):
-// false when (k, m, s, H) has none.
-bool find_protein_strip(int k, int m, int s, int H, const void **insert, const void **query, int *threads);
+// The protein and triplet alphabets' strip-kernel specialisations (shards
+// <= 2^31): false when (alphabet, k, m, s, H) has none.
+bool find_alphabet_strip(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
+                         int *threads);
 
 // Protein and DNA-triplet kernels, sbf_alphabet.cu: the compile-time
 // specialisation for (k, m, s, H) when there is one (*specialized = true),

@@ -274,11 +274,13 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int K_, int M_, int S_, int H_, int A_ = 0>
 struct StripCfg {
     static constexpr int K = K_, M = M_, S = S_, H = H_, A = A_;
-    static constexpr int BITS = A == 0 ? 2 : 5;         // bits per symbol
+    static constexpr int BITS = A == 0 ? 2 : A == 1 ? 5 : 6;  // bits per symbol
     static constexpr int W = K - M + 1;                 // m-mer windows per k-mer; block length
     static constexpr int Z = K - S;                     // s-mers per k-mer minus one
-    // blocks per strip (protein: ~110 k-mers, so that four query CTAs fit an SM)
-    static constexpr int NB = A != 0 ? (110 + W - 1) / W : (W >= 16) ? 8 : (128 + W - 1) / W;
+    // blocks per strip (protein: ~110 k-mers so that four query CTAs fit an
+    // SM; triplets: at most 60 per frame pass)
+    static constexpr int NB = A == 2 ? 60 / W : A == 1 ? (110 + W - 1) / W
+                                                           : (W >= 16) ? 8 : (128 + W - 1) / W;
     static constexpr int L = NB * W;                    // k-mers per thread
     static constexpr int NT = 128;                      // threads per CTA
     static constexpr int TILE = NT * L;                 // k-mer positions per tile (multiple of 32)
@@ -287,9 +289,19 @@ struct StripCfg {
     static constexpr int BIT_WORDS = (CODE_WORDS + 1) / 2 + 2;   // one bit per code index
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
     static constexpr int SLOTS = A == 0 ? 6 : 4;        // query: staged shards per thread per block
-    static constexpr int RAW_BYTES = 16 * CODE_WORDS;   // a tile's bytes, staged by one bulk copy
+    // Triplets (A = 2): a tile covers BYTE_TILE = 3 * TILE bytes in three frame
+    // passes; symbol c of pass f is the codon at byte T0 - OFF + f + 3c.
+    static constexpr int BYTE_TILE = A == 2 ? 3 * TILE : TILE;
+    static constexpr int OFF = A == 2 ? 48 : 16;        // bytes before T0 (16 symbols)
+    static constexpr int CODE_SYMS = 16 * CODE_WORDS;   // symbols per tile (pass)
+    // a tile's bytes, staged by one bulk copy
+    static constexpr int RAW_BYTES = A == 2 ? ((3 * CODE_SYMS + 4 + 15) / 16) * 16 : 16 * CODE_WORDS;
+    static constexpr int BYTE_WORDS = A == 2 ? RAW_BYTES / 32 + 2 : 1;  // byte-space boundary bitmap
+    static constexpr int OUT_WORDS = BYTE_TILE / 32;    // answer words per tile
     static_assert(W >= 1 && W <= 32 && Z >= 0 && H >= 1 && H <= kMaxH, "parameters");
     static_assert(A == 0 || BITS * K <= 64, "a k-mer packs into one 64-bit word");
+    static_assert(BYTE_TILE % 32 == 0, "tile must cover whole output words");
+    static_assert(A != 2 || L <= 64, "a triplet strip's validity bits are read as one 64-bit window");
     static_assert(TILE % 32 == 0, "tile must cover whole output words");
 };
 
@@ -300,12 +312,21 @@ struct StripSmem {
     uint16_t bad16[2 * C::BIT_WORDS];   // bit per code index; read as uint32 words
     uint32_t starts[C::BIT_WORDS];      // record-start bit per code index
     uint32_t valid[C::TILE_WORDS + 2];  // validity bit per k-mer of the tile
-    uint32_t outw[C::TILE_WORDS + 2];   // query answer bits of the tile
+    uint32_t outw[C::OUT_WORDS + 2];    // query answer bits of the tile
+    // triplets: record boundaries by byte, the highest boundary at or below the
+    // end of each byte word (relative to T0 - OFF, -1 if none in the tile), the
+    // in-frame bit per symbol of the current pass, the last boundary <= T0 - OFF
+    uint32_t bstarts[C::BYTE_WORDS];
+    int lastb[C::BYTE_WORDS];
+    uint32_t frame[A == 2 ? C::BIT_WORDS : 1];
+    int64_t prev_start;
+    int scan_tmp[4];
     uint2 onehot[64];                   // halves of 1 << p, p = 0 .. 63
     uint64_t raw_bar;                                   // completes the raw bulk copy
     int abort_flag;
     alignas(16) unsigned char raw[C::RAW_BYTES];        // the tile's sequence bytes (bulk copy)
-    alignas(16) uint8_t pcode[A == 0 ? 16 : C::RAW_BYTES];  // protein: one 5-bit code per byte
+    // protein: one 5-bit code per byte; triplets: one 6-bit codon code per symbol of the pass
+    alignas(16) uint8_t pcode[A == 0 ? 16 : A == 1 ? C::RAW_BYTES : C::CODE_SYMS];
 };
 
 
@@ -341,6 +362,8 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     using C = StripCfg<K, M, S, H, A>;
     constexpr int W = C::W, Z = C::Z, NB = C::NB, L = C::L, NT = C::NT, TILE = C::TILE;
     constexpr int R = C::SLOTS, BITS = C::BITS;
+    constexpr int BT = C::BYTE_TILE, OFF = C::OFF, NPASS = A == 2 ? 3 : 1;
+    constexpr int64_t kNone = INT64_MIN;
     constexpr uint64_t kMaskM = A == 0 ? 0ull : (1ull << (BITS * M)) - 1ull;
     constexpr uint64_t kMaskS = A == 0 ? 0ull : (1ull << (BITS * S)) - 1ull;
     __shared__ StripSmem<K, M, S, H, A> sm;
@@ -351,7 +374,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
     if (hi <= lo) return;
     const int64_t base = lo & ~int64_t(31);
-    const int64_t n_tiles = (hi - base + TILE - 1) / TILE;
+    const int64_t n_tiles = (hi - base + BT - 1) / BT;
     const int tid = threadIdx.x;
     const bool aligned = ((reinterpret_cast<uintptr_t>(a.seq)) & 15u) == 0;
     const uint32_t smask = (uint32_t)a.shard_mask;
@@ -362,7 +385,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     // one bulk copy (TMA) issued while the previous tile computes; other tiles
     // (the batch's edges, or an unaligned seq) load their bytes directly.
     auto bulk_ok = [&](int64_t tl) {
-        const int64_t a0 = base + tl * TILE - 16;
+        const int64_t a0 = base + tl * BT - OFF;
         return a.device_seq && aligned && a0 >= lo && a0 + C::RAW_BYTES <= hi;
     };
     if (tid == 0) {
@@ -374,16 +397,32 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     __syncthreads();
     uint32_t raw_phase = 0;
     if (tid == 0 && blockIdx.x < n_tiles && bulk_ok(blockIdx.x))
-        bulk_load(sm.raw, a.seq + (base + (int64_t)blockIdx.x * TILE - 16), C::RAW_BYTES, &sm.raw_bar);
+        bulk_load(sm.raw, a.seq + (base + (int64_t)blockIdx.x * BT - OFF), C::RAW_BYTES, &sm.raw_bar);
 
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int64_t T0 = base + tile * TILE;
-        const int64_t A0 = T0 - 16;  // absolute position of code index 0
+        const int64_t T0 = base + tile * BT;
+        const int64_t A0 = T0 - OFF;  // absolute position of code index 0 (triplets: of byte 0)
         const bool staged = bulk_ok(tile);
         // ---- phase 1 (warps 1..): bases -> codes + invalid bits.
         //      phase 1 (warp 0): record starts inside (T0, T0 + TILE + K - 1),
         //      from a search of the offsets, overlapping the others' encoding.
-        if (tid < 32) {
+        if (tid < 32 && A == 2) {
+            // triplets: every record boundary in (A0, A0 + RAW_BYTES) by byte,
+            // and the last boundary at or below A0
+            for (int w = tid; w < C::BYTE_WORDS; w += 32) sm.bstarts[w] = 0u;
+            if (tid < 2) sm.valid[C::TILE_WORDS + tid] = 0u;
+            const int64_t r0 = warp_find_boundary(a.offsets, a.n, A0, lo, hi, tid);
+            if (tid == 0) sm.prev_start = r0 >= 1 ? a.offsets[r0 - 1] : kNone;
+            __syncwarp();
+            const int64_t lim = A0 + C::RAW_BYTES;
+            bool more = true;
+            for (int64_t rb = r0; more; rb += 32) {
+                const int64_t r = rb + tid;
+                const int64_t p = r <= a.n ? a.offsets[r] : lim;
+                if (p > A0 && p < lim) atomicOr(&sm.bstarts[(p - A0) >> 5], 1u << ((p - A0) & 31));
+                more = __shfl_sync(0xffffffffu, p, 31) < lim && rb + 32 <= a.n;
+            }
+        } else if (tid < 32) {
             for (int w = tid; w < C::BIT_WORDS; w += 32) sm.starts[w] = 0u;
             if (tid < 2) sm.valid[C::TILE_WORDS + tid] = 0u;
             const int64_t r0 = warp_find_boundary(a.offsets, a.n, T0, lo, hi, tid);
@@ -408,8 +447,19 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
             }
         } else {
             if (kQuery)
-                for (int w = tid - 32; w < C::TILE_WORDS + 2; w += NT - 32) sm.outw[w] = 0u;
-            if (staged) {
+                for (int w = tid - 32; w < C::OUT_WORDS + 2; w += NT - 32) sm.outw[w] = 0u;
+            if (A == 2) {
+                // triplets: the raw bytes are the front end's output (codons are
+                // formed per frame pass below)
+                if (staged) {
+                    if (!mbar_wait(&sm.raw_bar, raw_phase)) sm.abort_flag = 1;
+                } else {
+                    for (int u = tid - 32; u < C::RAW_BYTES; u += NT - 32) {
+                        const int64_t pp = A0 + u;
+                        sm.raw[u] = (pp >= lo && pp < hi) ? a.seq[pp] : (unsigned char)0;
+                    }
+                }
+            } else if (staged) {
                 if (!mbar_wait(&sm.raw_bar, raw_phase)) sm.abort_flag = 1;
                 for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(sm.raw + 16 * c);
@@ -459,29 +509,126 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                     sm.bad16[c] = (uint16_t)bad;
                 }
             }
-            for (int c = C::CODE_WORDS + tid - 32; c < 2 * C::BIT_WORDS; c += NT - 32) sm.bad16[c] = 0xFFFFu;
+            if (A != 2)
+                for (int c = C::CODE_WORDS + tid - 32; c < 2 * C::BIT_WORDS; c += NT - 32) sm.bad16[c] = 0xFFFFu;
         }
         if (staged) raw_phase ^= 1u;
         if (__syncthreads_or(sm.abort_flag)) {
             if (tid == 0) atomicOr(a.status, kStatusTimeout);
             return;
         }
-        // the raw buffer is free again: start the next tile's copy
-        if (tid == 0 && tile + gridDim.x < n_tiles && bulk_ok(tile + gridDim.x))
-            bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * TILE - 16), C::RAW_BYTES, &sm.raw_bar);
+        // the raw buffer is free again (triplets: after the last frame pass's
+        // symbols are formed): start the next tile's copy
+        auto next_copy = [&]() {
+            if (tid == 0 && tile + gridDim.x < n_tiles && bulk_ok(tile + gridDim.x))
+                bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * BT - OFF), C::RAW_BYTES, &sm.raw_bar);
+        };
+        if constexpr (A != 2) next_copy();
+        int prev_res = -1;  // triplets: (A0 - last boundary <= A0) mod 3, -1 if none
+        if constexpr (A == 2) {
+            // highest boundary at or below the end of each byte word (a block
+            // max-scan; -1 = none since A0)
+            constexpr int PER = (C::BYTE_WORDS + NT - 1) / NT;
+            const int lane = tid & 31, warp = tid >> 5;
+            int loc[PER];
+            int run = -1;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int w = tid * PER + j;
+                if (w < C::BYTE_WORDS) {
+                    const uint32_t x = sm.bstarts[w];
+                    if (x) run = 32 * w + 31 - __clz(x);
+                }
+                loc[j] = run;
+            }
+            int incl = run;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl = v > incl ? v : incl;
+            }
+            if (lane == 31) sm.scan_tmp[warp] = incl;
+            __syncthreads();
+            int carry = -1;
+            for (int q = 0; q < warp; ++q) carry = sm.scan_tmp[q] > carry ? sm.scan_tmp[q] : carry;
+            const int up = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane > 0) carry = up > carry ? up : carry;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int w = tid * PER + j;
+                if (w < C::BYTE_WORDS) sm.lastb[w] = loc[j] > carry ? loc[j] : carry;
+            }
+            if (sm.prev_start != kNone) prev_res = (int)((A0 - sm.prev_start) % 3);
+            __syncthreads();
+        }
+
+        for (int pass = 0; pass < NPASS; ++pass) {
+        if constexpr (A == 2) {
+            // ---- phase 2 (triplets): symbol c of this pass is the codon at byte
+            // b = pass + 3c; invalid if a base is invalid or a record boundary
+            // falls inside it; `starts` marks a boundary at b; `frame` marks b
+            // in frame (the last boundary at or below b is a multiple of 3 back)
+            const int lane = tid & 31;
+            for (int c0 = (tid >> 5) * 32; c0 < 32 * C::BIT_WORDS; c0 += NT) {
+                const int c = c0 + lane;
+                uint32_t code = 63u;
+                bool bad = true, at = false, fr = false;
+                if (c < C::CODE_SYMS) {
+                    const int b = pass + 3 * c;
+                    const int x = base_code(sm.raw[b]), y = base_code(sm.raw[b + 1]), z = base_code(sm.raw[b + 2]);
+                    const uint32_t wb = sm.bstarts[b >> 5];
+                    const uint64_t two = (uint64_t)wb | ((uint64_t)sm.bstarts[(b >> 5) + 1] << 32);
+                    const bool inner = ((two >> ((b & 31) + 1)) & 3ull) != 0;
+                    bad = (x | y | z) < 0 || inner;
+                    if (!bad) code = (uint32_t)(x * 16 + y * 4 + z);
+                    at = (wb >> (b & 31)) & 1u;
+                    const uint32_t below = wb & (0xFFFFFFFFu >> (31 - (b & 31)));
+                    const int lb = below ? 32 * (b >> 5) + 31 - __clz(below)
+                                         : ((b >> 5) > 0 ? sm.lastb[(b >> 5) - 1] : -1);
+                    fr = lb >= 0 ? (b - lb) % 3 == 0 : (prev_res >= 0 && (b + prev_res) % 3 == 0);
+                    sm.pcode[c] = (uint8_t)code;
+                }
+                const unsigned bw = __ballot_sync(0xffffffffu, bad);
+                const unsigned aw = __ballot_sync(0xffffffffu, at);
+                const unsigned fw = __ballot_sync(0xffffffffu, fr);
+                if (lane == 0) {
+                    reinterpret_cast<uint32_t *>(sm.bad16)[c0 >> 5] = bw;
+                    sm.starts[c0 >> 5] = aw;
+                    sm.frame[c0 >> 5] = fw;
+                }
+            }
+            __syncthreads();
+            if (pass == NPASS - 1) next_copy();
+        }
         // ---- phase 3: validity bit per k-mer: no invalid base in its k bases,
-        // no record start among its bases 1 .. k-1.
+        // no record start among its bases 1 .. k-1 (triplets: and in frame).
         for (int v = tid; v < C::TILE_WORDS; v += NT) {
             const uint64_t badw = bits64_at(bad32, 32 * v + 16);
             const uint64_t stw = bits64_at(sm.starts, 32 * v + 17);
-            sm.valid[v] = ~(window_or<K>(badw) | window_or<K - 1>(stw));
+            uint32_t ok = ~(window_or<K>(badw) | window_or<K - 1>(stw));
+            if constexpr (A == 2) ok &= (uint32_t)bits64_at(sm.frame, 32 * v + 16);
+            sm.valid[v] = ok;
         }
         __syncthreads();
 
         // ---- phase 4: strips
         const int kk0 = tid * L;  // first k-mer of this thread (tile relative)
-        if (T0 + kk0 < hi) {
-            const unsigned am = __activemask();  // the lanes that own a strip in this tile
+        // (triplets: the strip's first k-mer starts at byte T0 + pass + 3 kk0)
+        const bool own = T0 + (A == 2 ? pass + 3 * kk0 : kk0) < hi;
+        bool go = own;
+        if constexpr (A == 2) {
+            // a warp skips a frame pass in which none of its strips holds a
+            // valid k-mer (inside one long record, two passes of three are out
+            // of frame)
+            // (every lane votes: a lane without a strip must not skip the vote)
+            const bool has = own && (bits64_at(sm.valid, kk0) & ((1ull << L) - 1ull)) != 0;
+            const bool any = __any_sync(0xffffffffu, has);
+            go = own && any;
+        }
+        // the lanes that run a strip, from a vote of the whole warp (the
+        // member mask of the cooperative flushes)
+        const unsigned am = __ballot_sync(0xffffffffu, go);
+        if (go) {
             // m-mer u of the strip starts at code index kk0 + 15 + u; the strip's
             // k-mers are u = 1 .. L (k-mer kk0 + u - 1 starts at code index kk0 + 16 + u - 1).
             uint64_t suf[W];
@@ -662,9 +809,17 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                         }
                     }
                     if (kQuery && present) {
-                        const int wi = kb >> 5, sh = kb & 31;
-                        atomicOr(&sm.outw[wi], present << sh);
-                        if (sh + W > 32) atomicOr(&sm.outw[wi + 1], (uint32_t)((uint64_t)present >> (32 - sh)));
+                        if constexpr (A == 2) {
+                            // k-mer kb + i starts at tile byte pass + 3 (kb + i)
+                            for (uint32_t pm = present; pm; pm &= pm - 1u) {
+                                const int rb = pass + 3 * (kb + __ffs(pm) - 1);
+                                atomicOr(&sm.outw[rb >> 5], 1u << (rb & 31));
+                            }
+                        } else {
+                            const int wi = kb >> 5, sh = kb & 31;
+                            atomicOr(&sm.outw[wi], present << sh);
+                            if (sh + W > 32) atomicOr(&sm.outw[wi + 1], (uint32_t)((uint64_t)present >> (32 - sh)));
+                        }
                     }
                 }
             }
@@ -677,9 +832,10 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
             }
         }
         __syncthreads();
+        }  // frame passes
         if (kQuery) {
             const int64_t w_lo = lo >> 5, w_hi = (hi + 31) >> 5;
-            for (int w = tid; w < C::TILE_WORDS; w += NT) {
+            for (int w = tid; w < C::OUT_WORDS; w += NT) {
                 const int64_t gw = (T0 >> 5) + w;
                 if (gw >= w_lo && gw < w_hi) a.out[gw] = sm.outw[w];
             }
