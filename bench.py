@@ -128,9 +128,9 @@ ALU_PEAK_TOPS = 152 * 64 * 2.07e9 / 1e12
 # the full-size launches of each workload (summaries under profiles/), valid
 # only for the kernel source they were measured on.
 MEASURED_TRAFFIC = {
-    "out-of-cache": {"source_sha": "3c3145b5b636cbd5", "insert": 14.4140, "query": 20.7756},
-    "protein-like": {"source_sha": "3c3145b5b636cbd5", "insert": 37.0068, "query": 52.7181},
-    "triplet": {"source_sha": "de8c4f435cbba80f", "insert": 32.9672, "query": 40.3194},
+    "out-of-cache": {"source_sha": "b9f6e9e71a406bdb", "insert": 14.4166, "query": 20.7731},
+    "protein-like": {"source_sha": "b9f6e9e71a406bdb", "insert": 37.0015, "query": 52.6958},
+    "triplet": {"source_sha": "4a990342684ce7df", "insert": 33.4197, "query": 40.3178},
 }
 
 
