@@ -180,3 +180,62 @@ def test_host_entry_points(torch, alphabet, params, mode):
     out = sbf.query_host(qry.seq, qry.offsets)
     assert_words_equal(out, oracle_answers(F, qry.seq, qry.offsets, params, 21, alphabet=alphabet),
                        qry.offsets)
+
+
+def test_protein_fasta_and_fastq_files(torch, tmp_path):
+    """Protein records through the file entry points: sbf_insert_fastx of a
+    FASTA file and sbf_query_fastx of a FASTQ file equal the oracle on the
+    same records (the reader keeps every byte of a sequence line)."""
+    import ctypes
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(74)
+    ins = _records(rng, "protein", 60, 0, 900, 1)
+    recs = [ins.seq[ins.offsets[r]:ins.offsets[r + 1]].tobytes() for r in range(ins.n_records)]
+    fa = tmp_path / "prot.fa"
+    fa.write_bytes(b"".join(b">p%d\n%s\n" % (i, r) for i, r in enumerate(recs)))
+    sbf = _filter(1 << 16, PROTEIN, 31, "protein")
+    n_rec, n_res = N.sbf_insert_fastx(sbf.handle, str(fa), batch_bases=7_000)
+    assert (n_rec, n_res) == (len(recs), int(ins.offsets[-1]))
+    F = oracle_image(ins.seq, ins.offsets, PROTEIN, 1 << 16, 31, alphabet="protein")
+    assert_images_equal(sbf.to_numpy(), F)
+    q = _records(rng, "protein", 200, 0, 120, 1)
+    qrecs = [q.seq[q.offsets[r]:q.offsets[r + 1]].tobytes() for r in range(q.n_records)]
+    fq = tmp_path / "frags.fq"
+    fq.write_bytes(b"".join(b"@f%d\n%s\n+\n%s\n" % (i, r, b"I" * len(r)) for i, r in enumerate(qrecs)))
+    got = []
+
+    def sink(s, o, n, b):
+        offs = np.ctypeslib.as_array((ctypes.c_int64 * (n + 1)).from_address(o)).copy()
+        words = np.ctypeslib.as_array((ctypes.c_uint32 * ((int(offs[-1]) + 31) // 32 + 1)).from_address(b)).copy()
+        got.append((offs, words))
+        return 0
+
+    N.sbf_query_fastx(sbf.handle, str(fq), sink, batch_bases=3_000)
+    pos = 0
+    for offs, words in got:
+        n = offs.size - 1
+        batch = qrecs[pos:pos + n]
+        pos += n
+        bseq = np.frombuffer(b"".join(batch), dtype=np.uint8) if batch else np.zeros(0, np.uint8)
+        assert_words_equal(words, oracle_answers(F, bseq, offs, PROTEIN, 31, alphabet="protein"), offs)
+    assert pos == len(qrecs)
+
+
+def test_triplet_noalloc_query(torch):
+    """sbf_query_host_noalloc on a triplet filter equals the oracle (the
+    no-alloc path stages the batch and runs the filter's own query kernel)."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    L = N.load()
+    rng = np.random.default_rng(75)
+    ins = _records(rng, "dna_triplet", 40, 0, 3000, 1)
+    qry = _with_own(ins, _records(rng, "dna_triplet", 60, 0, 500, 1))
+    sbf = _filter(1 << 16, TRIPLET, 41, "dna_triplet")
+    sbf.insert_host(ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, TRIPLET, 1 << 16, 41, alphabet="dna_triplet")
+    assert_images_equal(sbf.to_numpy(), F)
+    got = np.full((int(qry.offsets[-1]) + 31) // 32 + 1, 0xDEADBEEF, dtype=np.uint32)
+    rc = L.sbf_query_host_noalloc(sbf.handle, qry.seq.ctypes.data, qry.offsets.ctypes.data, qry.n_records,
+                                  got.ctypes.data, None)
+    assert rc == N.SBF_OK, N.last_error()
+    assert_words_equal(got, oracle_answers(F, qry.seq, qry.offsets, TRIPLET, 41, alphabet="dna_triplet"),
+                       qry.offsets)
