@@ -432,6 +432,25 @@ def main():
 
     words = out.cpu().numpy().view(np.uint32)
     fpr = fpr_of(words, qry, p["k"], B)
+
+    # the query batch as a dense record batch (all reads of one length, DNA):
+    # sbf_query_dense, timed apart from the step, its answers checked equal
+    dense = None
+    lens = np.diff(qry.offsets)
+    if p["alphabet"] == "dna" and lens.size and (lens == lens[0]).all() and qry.offsets[0] == 0:
+        rl = int(lens[0])
+        dout = torch.zeros_like(out)
+
+        def dq_call():
+            N.sbf_query_dense(sbf.handle, dq.data_ptr(), n_q, rl, dout.data_ptr(), sh)
+        t_dense = _timed(torch, dq_call, warmup=2, reps=max(args.steps, 3))
+        same = bool(torch.equal(dout[: (qry.n_bases + 31) // 32], out[: (qry.n_bases + 31) // 32]))
+        dense = {"call": "sbf_query_dense", "record_len": rl, "kmers_per_s": nk_q / t_dense,
+                 "ms": 1e3 * t_dense, "answers_equal_csr": same,
+                 "alu_frac": alu_ops(p)["query"] * nk_q / t_dense / 1e12 / ALU_PEAK_TOPS,
+                 "note": "one strip per read (skips the k-1 tail positions of each read); "
+                         "not part of `value`, which uses the CSR query"}
+        del dout
     value = throughput(world, args.steps, nk_ins + nk_q, total)
 
     # rooflines: insert against HBM (one 32-byte sector read and written per
@@ -508,6 +527,7 @@ def main():
             "insert_kmers_per_s": throughput(world, args.steps, nk_ins, s_ins),
             "query_kmers_per_s": throughput(world, args.steps, nk_q, s_q),
             "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
+            "query_dense": dense,
             "roofline": roofline, "roofline_other_kernel": roofline_other,
             "gpu_launches": 4 * args.steps,
             "gpu_launches_note": "per step: offsets check + insert kernel, offsets check + query kernel",

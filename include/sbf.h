@@ -232,6 +232,21 @@ int sbf_copy_bits(const sbf_filter *f, void *dst, uint64_t dst_bytes, void *stre
  * device memory).  Saves a filter together with sbf_copy_bits.  Async. */
 int sbf_load_bits(sbf_filter *f, const void *src, uint64_t src_bytes, void *stream);
 
+/* Query a dense record batch (Sec. IV-A's "dense record batches"): n_records
+ * records of record_len bytes each, back to back, record r = seq[r*record_len,
+ * (r+1)*record_len); seq is a device pointer to n_records*record_len bytes and
+ * no offsets array is read.  The answers are those of sbf_query with offsets
+ * r*record_len, in the same layout: out_bits (device, at least
+ * ceil(n_records*record_len / 32) words) gets bit g for the k-mer starting at
+ * byte g, every word in [0, ceil(n_records*record_len / 32)) is written.
+ * DNA filters only.  For record_len <= 160 and a filter at k=31, m=16, s=28,
+ * H=4 with at most 2^31 shards the query runs one strip per record, which
+ * skips the k-1 positions at each record's end that start no k-mer; otherwise
+ * it runs the runtime-parameter kernel.  Asynchronous on `stream`; no offsets
+ * check is needed, so the sticky status is not involved. */
+int sbf_query_dense(const sbf_filter *f, const char *seq, int64_t n_records, int64_t record_len,
+                    uint32_t *out_bits, void *stream);
+
 /* Zero the image (an empty filter).  Asynchronous on `stream`. */
 int sbf_clear(sbf_filter *f, void *stream);
 

@@ -23,6 +23,7 @@ _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "sbf_create": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64]),
     "sbf_create_alphabet": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64, _i32]),
+    "sbf_query_dense": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "sbf_get_alphabet": (_i32, [_vp]),
     "sbf_destroy": (None, [_vp]),
     "sbf_insert": (_i32, [_vp, _vp, _vp, _i64, _vp]),
@@ -175,6 +176,10 @@ def sbf_create_alphabet(num_bits: int, k: int, m: int, s: int, H: int, seed: int
     if not h:
         raise SBFError(SBF_ERR_INVALID_ARG, "sbf_create_alphabet", last_error())
     return h
+
+
+def sbf_query_dense(f: int, seq: int, n_records: int, record_len: int, out_bits: int, stream: int = 0) -> None:
+    check(load().sbf_query_dense(f, seq, n_records, record_len, out_bits, stream), "sbf_query_dense")
 
 
 def sbf_get_alphabet(f: int) -> int:

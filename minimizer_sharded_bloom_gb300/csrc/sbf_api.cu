@@ -139,6 +139,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.s = f->s;
     la.H = f->H;
     la.device_seq = device_seq ? 1 : 0;
+    la.rec_len = 0;
     return la;
 }
 
@@ -290,6 +291,10 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     f->threads_query = threads_query;
     f->grid_insert = grid_for(ins, threads, sms);
     f->grid_query = grid_for(qry, threads_query, sms);
+    if (alphabet == SBF_ALPHABET_DNA && shards <= (1ull << 31)) {
+        f->dense_query_kernel = sbf::dense_query_kernel(k, m, s, H, &f->threads_dense);
+        if (f->dense_query_kernel) f->grid_dense = grid_for(f->dense_query_kernel, f->threads_dense, sms);
+    }
     f->grid_check = 4 * sms;
     return f;
 }
@@ -337,6 +342,24 @@ int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int6
     if (n == 0) return SBF_OK;
     if (int rc = check_device(f)) return rc;
     return sbf::launch_query(f, seq, offsets, n, out_bits, stream, true);
+}
+
+int sbf_query_dense(const sbf_filter *f, const char *seq, int64_t n_records, int64_t record_len,
+                    uint32_t *out_bits, void *stream) {
+    if (!f || !seq || !out_bits || n_records < 0 || record_len < 1)
+        return fail(SBF_ERR_INVALID_ARG, "sbf_query_dense: bad arguments");
+    if (f->alphabet != SBF_ALPHABET_DNA) return fail(SBF_ERR_INVALID_ARG, "sbf_query_dense: DNA filters only");
+    if (n_records == 0) return SBF_OK;
+    if (n_records > (int64_t(1) << 40) / record_len)
+        return fail(SBF_ERR_INVALID_ARG, "sbf_query_dense: batch too large");
+    if (int rc = check_device(f)) return rc;
+    sbf::LaunchArgs la = make_args(f, seq, nullptr, n_records, out_bits, true);
+    la.rec_len = record_len;
+    // one record per strip when the filter has a dense strip kernel and the
+    // records fit it; the runtime-parameter kernel otherwise
+    if (f->dense_query_kernel && record_len <= sbf::kDenseMax)
+        return launch(f->dense_query_kernel, f->grid_dense, f->threads_dense, la, as_stream(stream));
+    return launch(sbf::generic_query_kernel(), f->grid_check * 2, 256, la, as_stream(stream));
 }
 
 int sbf_copy_bits(const sbf_filter *f, void *dst, uint64_t dst_bytes, void *stream) {

@@ -30,6 +30,8 @@ struct LaunchArgs {
     uint64_t seed;            // minimizer seed; the s-mer seed is ~seed
     int k, m, s, H;
     int device_seq;           // 1: seq is device memory (tile bytes may use TMA bulk copies)
+    int64_t rec_len;          // > 0: a dense batch, record r = seq[r*rec_len, (r+1)*rec_len)
+                              // and `offsets` is unused; 0: CSR offsets
 };
 
 // Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an

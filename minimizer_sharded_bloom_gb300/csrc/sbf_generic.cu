@@ -1,9 +1,10 @@
 // sbf_generic.cu -- runtime-parameter SBF kernels (any 1 <= m, s <= k <= 32,
-// 1 <= H <= 10), used for (k, m, s, H) combinations that have no compile-time
-// specialised kernel.  One thread per k-mer position, following the paper's
-// Algorithm 1 (insert) and Algorithm 2 (query) directly: pack the k-mer, take
-// the minimum minimizer hash over its k-m+1 m-mers, OR or test the bits of its
-// k-s+1 s-mers ("cuSBF", Sec. IV-D, IV-E).
+// 1 <= H <= 32; CSR batches or dense batches of fixed-length records), used
+// for (k, m, s, H) combinations that have no compile-time specialised kernel.
+// One thread per k-mer position, following the paper's Algorithm 1 (insert)
+// and Algorithm 2 (query) directly: pack the k-mer, take the minimum minimizer
+// hash over its k-m+1 m-mers, OR or test the bits of its k-s+1 s-mers
+// ("cuSBF", Sec. IV-D, IV-E).
 //
 // Work layout: a grid-stride loop over 32-position chunks aligned to absolute
 // position multiples of 32, one warp per chunk, so that each query answer word
@@ -17,7 +18,7 @@ namespace {
 template <bool kQuery>
 __global__ void __launch_bounds__(256) generic_kernel(LaunchArgs a) {
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
-    const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
+    const int64_t lo = a.rec_len ? 0 : a.offsets[0], hi = a.rec_len ? a.n * a.rec_len : a.offsets[a.n];
     if (hi <= lo) return;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -29,13 +30,19 @@ __global__ void __launch_bounds__(256) generic_kernel(LaunchArgs a) {
         bool valid = false;
         uint64_t shard = 0, K[4] = {0, 0, 0, 0};
         if (g >= lo && g < hi) {
-            // the record holding g: first r with offsets[r + 1] > g
-            int64_t r_lo = 0, r_hi = a.n - 1;
-            while (r_lo < r_hi) {
-                const int64_t mid = r_lo + ((r_hi - r_lo) >> 1);
-                if (a.offsets[mid + 1] > g) r_hi = mid; else r_lo = mid + 1;
+            // the end of the record holding g (first r with offsets[r + 1] > g)
+            int64_t rec_end;
+            if (a.rec_len) {
+                rec_end = (g / a.rec_len + 1) * a.rec_len;
+            } else {
+                int64_t r_lo = 0, r_hi = a.n - 1;
+                while (r_lo < r_hi) {
+                    const int64_t mid = r_lo + ((r_hi - r_lo) >> 1);
+                    if (a.offsets[mid + 1] > g) r_hi = mid; else r_lo = mid + 1;
+                }
+                rec_end = a.offsets[r_lo + 1];
             }
-            if (g + a.k <= a.offsets[r_lo + 1]) {
+            if (g + a.k <= rec_end) {
                 uint64_t kv = 0;
                 bool ok = true;
                 for (int i = 0; i < a.k; ++i) {

@@ -17,6 +17,8 @@ struct sbf_filter {
     const void *query_kernel = nullptr;
     int threads = 256;          // threads per block of the insert kernel
     int threads_query = 256;    // ... and of the query kernel
+    const void *dense_query_kernel = nullptr;  // dense batches (strip kernel), if any
+    int threads_dense = 0, grid_dense = 0;
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
     bool specialized = false;

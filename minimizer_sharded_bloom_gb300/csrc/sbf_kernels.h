@@ -12,6 +12,11 @@ const void *generic_insert_kernel();
 const void *generic_query_kernel();
 __global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status);
 
+// Dense batches (fixed-length records): the strip-kernel query for records of
+// at most kDenseMax bytes at (k, m, s, H), or nullptr.
+constexpr int kDenseMax = 160;
+const void *dense_query_kernel(int k, int m, int s, int H, int *threads);
+
 // The protein and triplet alphabets' strip-kernel specialisations (shards
 // <= 2^31): false when (alphabet, k, m, s, H) has none.
 bool find_alphabet_strip(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,

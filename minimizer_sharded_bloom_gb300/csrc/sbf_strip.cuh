@@ -271,24 +271,27 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int K_, int M_, int S_, int H_, int A_ = 0>
+template <int K_, int M_, int S_, int H_, int A_ = 0, int D_ = 0>
 struct StripCfg {
     static constexpr int K = K_, M = M_, S = S_, H = H_, A = A_;
+    // D > 0: dense batches of fixed-length records of at most D bytes, one
+    // record per strip (DNA query); the sizes below are then maxima
+    static constexpr int D = D_;
     static constexpr int BITS = A == 0 ? 2 : A == 1 ? 5 : 6;  // bits per symbol
     static constexpr int W = K - M + 1;                 // m-mer windows per k-mer; block length
     static constexpr int Z = K - S;                     // s-mers per k-mer minus one
     // blocks per strip (protein: ~110 k-mers so that four query CTAs fit an
     // SM; triplets: at most 60 per frame pass)
-    static constexpr int NB = A == 2 ? 60 / W : A == 1 ? (110 + W - 1) / W
+    static constexpr int NB = D > 0 ? (D + W - 1) / W : A == 2 ? 60 / W : A == 1 ? (110 + W - 1) / W
                                                            : (W >= 16) ? 8 : (128 + W - 1) / W;
     static constexpr int L = NB * W;                    // k-mers per thread
     static constexpr int NT = 128;                      // threads per CTA
-    static constexpr int TILE = NT * L;                 // k-mer positions per tile (multiple of 32)
+    static constexpr int TILE = D > 0 ? NT * D : NT * L;  // k-mer positions per tile (multiple of 32)
     static constexpr int TILE_WORDS = TILE / 32;
     static constexpr int CODE_WORDS = (TILE + K + 96) / 16 + 4;  // 16 bases per word
     static constexpr int BIT_WORDS = (CODE_WORDS + 1) / 2 + 2;   // one bit per code index
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
-    static constexpr int SLOTS = A == 0 ? 6 : 4;        // query: staged shards per thread per block
+    static constexpr int SLOTS = A == 0 && D == 0 ? 6 : 4;  // query: staged shards per thread per block
     // Triplets (A = 2): a tile covers BYTE_TILE = 3 * TILE bytes in three frame
     // passes; symbol c of pass f is the codon at byte T0 - OFF + f + 3c.
     static constexpr int BYTE_TILE = A == 2 ? 3 * TILE : TILE;
@@ -305,9 +308,9 @@ struct StripCfg {
     static_assert(TILE % 32 == 0, "tile must cover whole output words");
 };
 
-template <int K, int M, int S, int H, int A = 0>
+template <int K, int M, int S, int H, int A = 0, int D = 0>
 struct StripSmem {
-    using C = StripCfg<K, M, S, H, A>;
+    using C = StripCfg<K, M, S, H, A, D>;
     uint32_t codes[A == 0 ? C::CODE_WORDS : 1];  // DNA: 16 2-bit codes per word
     uint16_t bad16[2 * C::BIT_WORDS];   // bit per code index; read as uint32 words
     uint32_t starts[C::BIT_WORDS];      // record-start bit per code index
@@ -357,24 +360,34 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const ui
     }
 }
 
-template <int K, int M, int S, int H, bool kQuery, int A = 0>
-__global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(LaunchArgs a) {
-    using C = StripCfg<K, M, S, H, A>;
+template <int K, int M, int S, int H, bool kQuery, int A = 0, int D = 0>
+__global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(LaunchArgs a) {
+    using C = StripCfg<K, M, S, H, A, D>;
     constexpr int W = C::W, Z = C::Z, NB = C::NB, L = C::L, NT = C::NT, TILE = C::TILE;
     constexpr int R = C::SLOTS, BITS = C::BITS;
     constexpr int BT = C::BYTE_TILE, OFF = C::OFF, NPASS = A == 2 ? 3 : 1;
     constexpr int64_t kNone = INT64_MIN;
     constexpr uint64_t kMaskM = A == 0 ? 0ull : (1ull << (BITS * M)) - 1ull;
     constexpr uint64_t kMaskS = A == 0 ? 0ull : (1ull << (BITS * S)) - 1ull;
-    __shared__ StripSmem<K, M, S, H, A> sm;
+    __shared__ StripSmem<K, M, S, H, A, D> sm;
     // query: shards of the current block's run heads, [slot][half][thread]
     __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
 
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
-    const int64_t lo = a.offsets[0], hi = a.offsets[a.n];
+    // dense batches: record r is bytes [r rlen, (r + 1) rlen), a tile holds NT
+    // records; the geometry below is runtime there and the constants otherwise
+    const int rlen = D > 0 ? (int)a.rec_len : 0;
+    const int tile_pos = D > 0 ? NT * rlen : BT;               // positions (bytes) per tile
+    const int code_words = D > 0 ? (tile_pos + K + 96) / 16 + 4 : C::CODE_WORDS;
+    const int raw_bytes = D > 0 ? 16 * code_words : C::RAW_BYTES;
+    const int tile_words = D > 0 ? tile_pos / 32 : C::TILE_WORDS;
+    const int strip_len = D > 0 ? rlen : L;
+    const int nbl = D > 0 ? (rlen - K + 1 + W - 1) / W : NB;  // blocks per strip
+    const int64_t lo = D > 0 ? 0 : a.offsets[0];
+    const int64_t hi = D > 0 ? a.n * (int64_t)rlen : a.offsets[a.n];
     if (hi <= lo) return;
     const int64_t base = lo & ~int64_t(31);
-    const int64_t n_tiles = (hi - base + BT - 1) / BT;
+    const int64_t n_tiles = (hi - base + tile_pos - 1) / tile_pos;
     const int tid = threadIdx.x;
     const bool aligned = ((reinterpret_cast<uintptr_t>(a.seq)) & 15u) == 0;
     const uint32_t smask = (uint32_t)a.shard_mask;
@@ -385,8 +398,8 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     // one bulk copy (TMA) issued while the previous tile computes; other tiles
     // (the batch's edges, or an unaligned seq) load their bytes directly.
     auto bulk_ok = [&](int64_t tl) {
-        const int64_t a0 = base + tl * BT - OFF;
-        return a.device_seq && aligned && a0 >= lo && a0 + C::RAW_BYTES <= hi;
+        const int64_t a0 = base + tl * tile_pos - OFF;
+        return a.device_seq && aligned && a0 >= lo && a0 + raw_bytes <= hi;
     };
     if (tid == 0) {
         mbar_init(&sm.raw_bar, 1);
@@ -397,10 +410,10 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
     __syncthreads();
     uint32_t raw_phase = 0;
     if (tid == 0 && blockIdx.x < n_tiles && bulk_ok(blockIdx.x))
-        bulk_load(sm.raw, a.seq + (base + (int64_t)blockIdx.x * BT - OFF), C::RAW_BYTES, &sm.raw_bar);
+        bulk_load(sm.raw, a.seq + (base + (int64_t)blockIdx.x * tile_pos - OFF), raw_bytes, &sm.raw_bar);
 
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int64_t T0 = base + tile * BT;
+        const int64_t T0 = base + tile * tile_pos;
         const int64_t A0 = T0 - OFF;  // absolute position of code index 0 (triplets: of byte 0)
         const bool staged = bulk_ok(tile);
         // ---- phase 1 (warps 1..): bases -> codes + invalid bits.
@@ -421,6 +434,15 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                 const int64_t p = r <= a.n ? a.offsets[r] : lim;
                 if (p > A0 && p < lim) atomicOr(&sm.bstarts[(p - A0) >> 5], 1u << ((p - A0) & 31));
                 more = __shfl_sync(0xffffffffu, p, 31) < lim && rb + 32 <= a.n;
+            }
+        } else if (tid < 32 && D > 0) {
+            // dense: record starts at T0 + j rlen (T0 is a multiple of rlen)
+            for (int w = tid; w < C::BIT_WORDS; w += 32) sm.starts[w] = 0u;
+            if (tid < 2) sm.valid[tile_words + tid] = 0u;
+            __syncwarp();
+            for (int j = tid + 1; j <= NT + 1; j += 32) {
+                const int ci = 16 + j * rlen;
+                if (ci < 16 + tile_pos + K - 1) atomicOr(&sm.starts[ci >> 5], 1u << (ci & 31));
             }
         } else if (tid < 32) {
             for (int w = tid; w < C::BIT_WORDS; w += 32) sm.starts[w] = 0u;
@@ -461,7 +483,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                 }
             } else if (staged) {
                 if (!mbar_wait(&sm.raw_bar, raw_phase)) sm.abort_flag = 1;
-                for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
+                for (int c = tid - 32; c < code_words; c += NT - 32) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(sm.raw + 16 * c);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                     uint32_t bad;
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                     sm.bad16[c] = (uint16_t)bad;
                 }
             } else {
-                for (int c = tid - 32; c < C::CODE_WORDS; c += NT - 32) {
+                for (int c = tid - 32; c < code_words; c += NT - 32) {
                     const int64_t p0 = A0 + 16 * (int64_t)c;
                     uint32_t w[4];
                     if (aligned && p0 >= lo && p0 + 16 <= hi) {
@@ -510,7 +532,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
                 }
             }
             if (A != 2)
-                for (int c = C::CODE_WORDS + tid - 32; c < 2 * C::BIT_WORDS; c += NT - 32) sm.bad16[c] = 0xFFFFu;
+                for (int c = code_words + tid - 32; c < 2 * C::BIT_WORDS; c += NT - 32) sm.bad16[c] = 0xFFFFu;
         }
         if (staged) raw_phase ^= 1u;
         if (__syncthreads_or(sm.abort_flag)) {
@@ -521,7 +543,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
         // symbols are formed): start the next tile's copy
         auto next_copy = [&]() {
             if (tid == 0 && tile + gridDim.x < n_tiles && bulk_ok(tile + gridDim.x))
-                bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * BT - OFF), C::RAW_BYTES, &sm.raw_bar);
+                bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * tile_pos - OFF), raw_bytes, &sm.raw_bar);
         };
         if constexpr (A != 2) next_copy();
         int prev_res = -1;  // triplets: (A0 - last boundary <= A0) mod 3, -1 if none
@@ -602,7 +624,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
         }
         // ---- phase 3: validity bit per k-mer: no invalid base in its k bases,
         // no record start among its bases 1 .. k-1 (triplets: and in frame).
-        for (int v = tid; v < C::TILE_WORDS; v += NT) {
+        for (int v = tid; v < tile_words; v += NT) {
             const uint64_t badw = bits64_at(bad32, 32 * v + 16);
             const uint64_t stw = bits64_at(sm.starts, 32 * v + 17);
             uint32_t ok = ~(window_or<K>(badw) | window_or<K - 1>(stw));
@@ -612,7 +634,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
         __syncthreads();
 
         // ---- phase 4: strips
-        const int kk0 = tid * L;  // first k-mer of this thread (tile relative)
+        const int kk0 = tid * strip_len;  // first k-mer of this thread (tile relative)
         // (triplets: the strip's first k-mer starts at byte T0 + pass + 3 kk0)
         const bool own = T0 + (A == 2 ? pass + 3 * kk0 : kk0) < hi;
         bool go = own;
@@ -675,7 +697,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
             uint64_t *const words = a.words;
 
 #pragma unroll 1
-            for (int blk = 0; blk <= NB; ++blk) {
+            for (int blk = 0; blk <= nbl; ++blk) {
                 // -- pass A: m-mers u = blk*W .. blk*W + W-1; emits the keys of
                 //    k-mers u = (blk-1)*W + 1 .. blk*W (the strip's block blk-1).
                 //    Query: every run head's shard is copied to a slot (cp.async)
@@ -835,7 +857,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A>::NT) strip_kernel(Laun
         }  // frame passes
         if (kQuery) {
             const int64_t w_lo = lo >> 5, w_hi = (hi + 31) >> 5;
-            for (int w = tid; w < C::OUT_WORDS; w += NT) {
+            for (int w = tid; w < (D > 0 ? tile_words : C::OUT_WORDS); w += NT) {
                 const int64_t gw = (T0 >> 5) + w;
                 if (gw >= w_lo && gw < w_hi) a.out[gw] = sm.outw[w];
             }

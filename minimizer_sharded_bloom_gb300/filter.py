@@ -92,6 +92,17 @@ class SuperBloomFilter:
         return out
 
     # ---- host-resident (synchronising) ------------------------------------
+    def query_dense(self, seq: torch.Tensor, record_len: int, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+        """Query a dense batch of fixed-length records (seq.numel() //
+        record_len of them); same answer layout as query()."""
+        _check_device_u8(seq)
+        n = seq.numel() // record_len
+        if out is None:
+            out = torch.zeros((n * record_len + 31) // 32 + 1, dtype=torch.int32, device=seq.device)
+        N.sbf_query_dense(self._h, seq.data_ptr(), n, record_len, out.data_ptr(), _stream_handle(stream))
+        return out
+
     def insert_host(self, seq: np.ndarray, offsets: np.ndarray) -> None:
         seq = np.ascontiguousarray(seq, dtype=np.uint8)
         offsets = np.ascontiguousarray(offsets, dtype=np.int64)

@@ -145,6 +145,13 @@ def test_out_of_cache_full(torch):
     del dseq, doff
     assert sbf.status() == 0
     words = _sampled_checks(torch, sbf, ins, qry, MAIN, seed, rng)
+    # the same reads as a dense batch (150 bp each) answer identically
+    dq, _ = to_dev(torch, qry.seq, qry.offsets)
+    dense = torch.zeros((int(qry.offsets[-1]) + 31) // 32 + 1, dtype=torch.int32, device="cuda")
+    sbf.query_dense(dq[: qry.seq.size], 150, out=dense)
+    torch.cuda.synchronize()
+    assert np.array_equal(dense.cpu().numpy().view(np.uint32)[: words.size], words)
+    del dq, dense
     # reads taken from the contigs without errors in a k-mer answer positive;
     # uniform reads give the false-positive rate (near 0 at 16 bits/k-mer).
     starts = qry.offsets[:-1][qry.meta["is_random"]][:20000]

@@ -209,6 +209,43 @@ def test_host_calls_report_bad_offsets(torch, mode):
     assert_words_equal(sbf.query_host(seq, good), oracle_answers(F, seq, good, MAIN, 4), good)
 
 
+@pytest.mark.parametrize("R,n,params", [
+    (31, 300, MAIN), (50, 129, MAIN), (120, 1000, MAIN), (150, 777, MAIN), (160, 128, MAIN),
+    (150, 1, MAIN), (30, 200, MAIN), (161, 300, MAIN), (400, 90, MAIN),
+    (150, 500, dict(k=25, m=11, s=20, H=3)), (100, 64, dict(k=31, m=16, s=28, H=12))])
+def test_dense_query_equals_csr_and_oracle(torch, R, n, params):
+    """sbf_query_dense on n fixed-length records of R bytes (N runs, lowercase;
+    partial last tile; an unaligned pointer for odd n) equals the oracle on
+    the same records as CSR offsets and the CSR query, word for word: the
+    dense strip kernel (R <= 160 at the operating point) and the
+    runtime-parameter fallback (shorter than k, longer than 160, other
+    parameters)."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng(900 + R + n)
+    ins = synth.random_records(rng, 60, 500, 8000, n_prob=0.002)
+    reads = synth.random_records(rng, n, R, R, n_prob=0.003, lower_prob=0.05)
+    half = reads.seq.reshape(n, R)[: n // 2]
+    take = min(ins.seq.size, half.size) // R * R
+    src = ins.seq[:take].reshape(-1, R)
+    half[: src.shape[0]] = src  # up to half the reads copied from the inserted records
+    seq = reads.seq
+    off = synth.csr(np.full(n, R))
+    sbf = _filter(1 << 18, params, 61)
+    gpu_insert(torch, sbf, ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, params, 1 << 18, 61)
+    pad = n % 2 * 3
+    dseq, _ = to_dev(torch, seq, off, pad)
+    words = (n * R + 31) // 32
+    out = torch.full((words + 2,), -1, dtype=torch.int32, device="cuda")
+    sbf.query_dense(dseq[: n * R], R, out=out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    assert (got[words:] == 0xFFFFFFFF).all()  # nothing past the answer range
+    want = oracle_answers(F, seq, off, params, 61)
+    assert_words_equal(got, want, off)
+    assert_words_equal(got, gpu_query(torch, sbf, seq, off), off)
+
+
 def test_filter_algebra_on_gpu(torch):
     """Order independence, split inserts, idempotence and union, on the GPU
     image (OR is commutative and idempotent)."""
