@@ -125,7 +125,13 @@ int sbf_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n
  * record, all k bases valid) and every bit of all its k-s+1 s-mers is set in
  * its shard.  Every word in [offsets[0] >> 5, (offsets[n] + 31) >> 5) is
  * written (positions without a valid k-mer get 0); other words are untouched.
- * Asynchronous on `stream`. */
+ * Asynchronous on `stream`.  Where the filter has a dense-batch kernel (the
+ * operating point k=31 m=16 s=28 H=4), a batch whose records all have one
+ * length R with k <= R <= 160 and offsets[0] == 0 runs as sbf_query_dense
+ * would run it, with identical answers; the call then takes one 4-byte
+ * stream-ordered allocation from a memory pool of the filter's own (kept
+ * between calls) for the device-side uniformity flag, and frees it on
+ * `stream`.  Concurrent queries of one filter on several streams are safe. */
 int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
               uint32_t *out_bits, void *stream);
 

@@ -115,9 +115,15 @@ int launch(const void *fn, int grid, int threads, const sbf::LaunchArgs &la, cud
     return SBF_OK;
 }
 
-int launch_check(const sbf_filter *f, const int64_t *offsets, int64_t n, cudaStream_t st) {
+int launch_check(const sbf_filter *f, const int64_t *offsets, int64_t n, cudaStream_t st,
+                 int *nonuniform = nullptr) {
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, f->grid_check);
-    sbf::check_offsets_kernel<<<(int)std::max<int64_t>(blocks, 1), 256, 0, st>>>(offsets, n, f->status);
+    if (nonuniform) {
+        cudaError_t e = cudaMemsetAsync(nonuniform, 0, sizeof(int), st);
+        if (e != cudaSuccess) return cuda_fail(e, "flag reset");
+    }
+    sbf::check_offsets_kernel<<<(int)std::max<int64_t>(blocks, 1), 256, 0, st>>>(offsets, n, f->status,
+                                                                                 nonuniform);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "offsets check launch");
     return SBF_OK;
@@ -140,6 +146,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.H = f->H;
     la.device_seq = device_seq ? 1 : 0;
     la.rec_len = 0;
+    la.nonuniform = nullptr;
     return la;
 }
 
@@ -179,12 +186,35 @@ int sbf::launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, i
 }
 
 int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
-                      uint32_t *out_bits, void *stream, bool device_seq) {
+                      uint32_t *out_bits, void *stream, bool device_seq, int *flag_word) {
     if (n == 0) return SBF_OK;
     cudaStream_t st = as_stream(stream);
-    if (int rc = launch_check(f, offsets, n, st)) return rc;
-    return launch(f->query_kernel, f->grid_query, f->threads_query,
-                  make_args(f, seq, offsets, n, out_bits, device_seq), st);
+    // Where the query kernel can run a uniform batch as a dense one, the
+    // offsets check reports uniformity into a word of this call's own (a
+    // stream-ordered allocation from the filter's pool, or the caller's), so
+    // that concurrent queries of one filter never share it.  Without a word
+    // the kernel keeps the CSR geometry, which is correct for every batch.
+    int *flag = nullptr;
+    bool owned = false;
+    if (f->query_detects_dense) {
+        if (flag_word) {
+            flag = flag_word;
+        } else if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&flag), sizeof(int), f->flag_pool, st) ==
+                   cudaSuccess) {
+            owned = true;
+        } else {
+            cudaGetLastError();
+            flag = nullptr;
+        }
+    }
+    int rc = launch_check(f, offsets, n, st, flag);
+    if (rc == SBF_OK) {
+        sbf::LaunchArgs la = make_args(f, seq, offsets, n, out_bits, device_seq);
+        la.nonuniform = flag;
+        rc = launch(f->query_kernel, f->grid_query, f->threads_query, la, st);
+    }
+    if (owned) cudaFreeAsync(flag, st);
+    return rc;
 }
 
 extern "C" {
@@ -293,7 +323,25 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     f->grid_query = grid_for(qry, threads_query, sms);
     if (alphabet == SBF_ALPHABET_DNA && shards <= (1ull << 31)) {
         f->dense_query_kernel = sbf::dense_query_kernel(k, m, s, H, &f->threads_dense);
-        if (f->dense_query_kernel) f->grid_dense = grid_for(f->dense_query_kernel, f->threads_dense, sms);
+        if (f->dense_query_kernel) {
+            f->grid_dense = grid_for(f->dense_query_kernel, f->threads_dense, sms);
+            if (f->dense_query_kernel == f->query_kernel) {
+                // the per-call uniformity words come from a pool of the
+                // filter's own that keeps its memory between calls
+                cudaMemPoolProps props = {};
+                props.allocType = cudaMemAllocationTypePinned;
+                props.location.type = cudaMemLocationTypeDevice;
+                props.location.id = f->device;
+                if (cudaMemPoolCreate(&f->flag_pool, &props) == cudaSuccess) {
+                    uint64_t keep = UINT64_MAX;
+                    cudaMemPoolSetAttribute(f->flag_pool, cudaMemPoolAttrReleaseThreshold, &keep);
+                    f->query_detects_dense = true;
+                } else {
+                    cudaGetLastError();
+                    f->flag_pool = nullptr;
+                }
+            }
+        }
     }
     f->grid_check = 4 * sms;
     return f;
@@ -308,6 +356,7 @@ void sbf_destroy(sbf_filter *f) {
     sbf::destroy_stager(f->stager);
     cudaFree(f->words);
     cudaFree(f->status);
+    if (f->flag_pool) cudaMemPoolDestroy(f->flag_pool);
     if (prev >= 0 && prev != f->device) cudaSetDevice(prev);
     delete f;
 }

@@ -32,6 +32,8 @@ struct LaunchArgs {
     int device_seq;           // 1: seq is device memory (tile bytes may use TMA bulk copies)
     int64_t rec_len;          // > 0: a dense batch, record r = seq[r*rec_len, (r+1)*rec_len)
                               // and `offsets` is unused; 0: CSR offsets
+    const int *nonuniform;    // CSR queries that may run as dense batches: nonzero when the
+                              // offsets check saw records of different lengths (else nullptr)
 };
 
 // Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an

@@ -90,14 +90,24 @@ const void *generic_insert_kernel() { return reinterpret_cast<const void *>(&gen
 const void *generic_query_kernel() { return reinterpret_cast<const void *>(&generic_kernel<true>); }
 
 // One thread per offsets pair; sets the sticky status on a decreasing pair or
-// a negative first offset.
-__global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status) {
+// a negative first offset.  With `nonuniform` (zeroed by the caller), also
+// flags a record whose length differs from the first record's.
+__global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status, int *nonuniform) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    bool bad = false;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride)
-        bad |= off[i + 1] < off[i];
+    const int64_t len0 = off[1] - off[0];
+    bool bad = false, uneven = false;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int64_t d = off[i + 1] - off[i];
+        bad |= d < 0;
+        uneven |= d != len0;
+    }
     if (blockIdx.x == 0 && threadIdx.x == 0) bad |= off[0] < 0;
-    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusBadOffsets);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    const bool any_uneven = __any_sync(0xffffffffu, uneven);
+    if ((threadIdx.x & 31) == 0) {
+        if (any_bad) atomicOr(status, kStatusBadOffsets);
+        if (any_uneven && nonuniform) atomicOr(nonuniform, 1);
+    }
 }
 
 }  // namespace sbf

@@ -1,6 +1,8 @@
 // sbf_internal.h -- the filter object and helpers shared by the C ABI units.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 
 #include "sbf.h"
@@ -18,6 +20,8 @@ struct sbf_filter {
     int threads = 256;          // threads per block of the insert kernel
     int threads_query = 256;    // ... and of the query kernel
     const void *dense_query_kernel = nullptr;  // dense batches (strip kernel), if any
+    bool query_detects_dense = false;          // query_kernel runs uniform CSR batches as dense
+    cudaMemPool_t flag_pool = nullptr;         // ... with a per-call flag word from this pool
     int threads_dense = 0, grid_dense = 0;
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
@@ -39,6 +43,8 @@ void destroy_stager(void *stager);
 // memory read in place (the kernel then loads tile bytes without TMA).
 int launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream,
                   bool device_seq);
+// flag_word: a device int the call may use to detect a uniform batch (the
+// no-alloc path passes one of its own); nullptr: allocated per call.
 int launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
-                 uint32_t *out_bits, void *stream, bool device_seq);
+                 uint32_t *out_bits, void *stream, bool device_seq, int *flag_word = nullptr);
 }  // namespace sbf

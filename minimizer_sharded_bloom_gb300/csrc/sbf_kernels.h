@@ -10,10 +10,12 @@ namespace sbf {
 // Runtime-parameter kernels (any valid k, m, s, H), sbf_generic.cu.
 const void *generic_insert_kernel();
 const void *generic_query_kernel();
-__global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status);
+__global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status, int *nonuniform);
 
 // Dense batches (fixed-length records): the strip-kernel query for records of
-// at most kDenseMax bytes at (k, m, s, H), or nullptr.
+// at most kDenseMax bytes at (k, m, s, H), or nullptr.  The same kernel is the
+// filter's CSR query there: it runs a CSR batch whose records all have one
+// length <= kDenseMax, starting at offset 0, as a dense batch.
 constexpr int kDenseMax = 160;
 const void *dense_query_kernel(int k, int m, int s, int H, int *threads);
 

@@ -30,9 +30,11 @@ constexpr int64_t kOffBytes = (kMaxRecords + 1) * 8;
 constexpr int64_t kOutBytes = (kMaxPositions / 32 + 8) * 4;
 constexpr int64_t kOffAt = (kSeqBytes + 255) & ~int64_t(255);
 constexpr int64_t kOutAt = (kOffAt + kOffBytes + 255) & ~int64_t(255);
-constexpr int64_t kScratchBytes = kOutAt + kOutBytes;
+constexpr int64_t kFlagAt = (kOutAt + kOutBytes + 255) & ~int64_t(255);
+constexpr int64_t kScratchBytes = kFlagAt + 256;
 
-// ~26 MiB: the sequence bytes, then the offsets, then the answer words.
+// ~26 MiB: the sequence bytes, then the offsets, then the answer words, then
+// the query's uniform-batch flag word.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -98,7 +100,8 @@ extern "C" int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, cons
     cudaError_t e = cudaMemcpyAsync(d_seq + (lo - cs), seq + lo, (size_t)(hi - lo), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(d_off, offsets, sizeof(int64_t) * (size_t)(n + 1), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return set_error(SBF_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
-    if (int rc = sbf_query(f, k_seq, d_off, n, k_out, stream)) return rc;
+    int *d_flag = reinterpret_cast<int *>(base + kFlagAt);
+    if (int rc = sbf::launch_query(f, k_seq, d_off, n, k_out, stream, true, d_flag)) return rc;
     e = cudaMemcpyAsync(out_bits + (cs >> 5), d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return set_error(SBF_ERR_CUDA, "sbf_query_host_noalloc: %s", cudaGetErrorString(e));

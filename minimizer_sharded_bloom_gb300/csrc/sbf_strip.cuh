@@ -375,16 +375,23 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
 
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
     // dense batches: record r is bytes [r rlen, (r + 1) rlen), a tile holds NT
-    // records; the geometry below is runtime there and the constants otherwise
-    const int rlen = D > 0 ? (int)a.rec_len : 0;
-    const int tile_pos = D > 0 ? NT * rlen : BT;               // positions (bytes) per tile
-    const int code_words = D > 0 ? (tile_pos + K + 96) / 16 + 4 : C::CODE_WORDS;
-    const int raw_bytes = D > 0 ? 16 * code_words : C::RAW_BYTES;
-    const int tile_words = D > 0 ? tile_pos / 32 : C::TILE_WORDS;
-    const int strip_len = D > 0 ? rlen : L;
-    const int nbl = D > 0 ? (rlen - K + 1 + W - 1) / W : NB;  // blocks per strip
-    const int64_t lo = D > 0 ? 0 : a.offsets[0];
-    const int64_t hi = D > 0 ? a.n * (int64_t)rlen : a.offsets[a.n];
+    // records; the geometry below is runtime there and the constants otherwise.
+    // A CSR batch runs dense too when the offsets check found every record of
+    // one length rlen (K <= rlen <= D) and the batch starts at offset 0.
+    int rlen = D > 0 ? (int)a.rec_len : 0;
+    if (D > 0 && rlen == 0 && a.nonuniform != nullptr && *a.nonuniform == 0) {
+        const int64_t o0 = a.offsets[0], len0 = a.offsets[1] - o0;
+        if (o0 == 0 && len0 >= K && len0 <= D) rlen = (int)len0;
+    }
+    const bool dense = D > 0 && rlen > 0;
+    const int tile_pos = dense ? NT * rlen : BT;               // positions (bytes) per tile
+    const int code_words = dense ? (tile_pos + K + 96) / 16 + 4 : C::CODE_WORDS;
+    const int raw_bytes = dense ? 16 * code_words : C::RAW_BYTES;
+    const int tile_words = dense ? tile_pos / 32 : C::TILE_WORDS;
+    const int strip_len = dense ? rlen : L;
+    const int nbl = dense ? (rlen - K + 1 + W - 1) / W : NB;  // blocks per strip
+    const int64_t lo = D > 0 && a.rec_len > 0 ? 0 : a.offsets[0];
+    const int64_t hi = D > 0 && a.rec_len > 0 ? a.n * (int64_t)rlen : a.offsets[a.n];
     if (hi <= lo) return;
     const int64_t base = lo & ~int64_t(31);
     const int64_t n_tiles = (hi - base + tile_pos - 1) / tile_pos;
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                 if (p > A0 && p < lim) atomicOr(&sm.bstarts[(p - A0) >> 5], 1u << ((p - A0) & 31));
                 more = __shfl_sync(0xffffffffu, p, 31) < lim && rb + 32 <= a.n;
             }
-        } else if (tid < 32 && D > 0) {
+        } else if (tid < 32 && dense) {
             // dense: record starts at T0 + j rlen (T0 is a multiple of rlen)
             for (int w = tid; w < C::BIT_WORDS; w += 32) sm.starts[w] = 0u;
             if (tid < 2) sm.valid[tile_words + tid] = 0u;
@@ -857,7 +864,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         }  // frame passes
         if (kQuery) {
             const int64_t w_lo = lo >> 5, w_hi = (hi + 31) >> 5;
-            for (int w = tid; w < (D > 0 ? tile_words : C::OUT_WORDS); w += NT) {
+            for (int w = tid; w < (dense ? tile_words : C::OUT_WORDS); w += NT) {
                 const int64_t gw = (T0 >> 5) + w;
                 if (gw >= w_lo && gw < w_hi) a.out[gw] = sm.outw[w];
             }

@@ -246,6 +246,94 @@ def test_dense_query_equals_csr_and_oracle(torch, R, n, params):
     assert_words_equal(got, gpu_query(torch, sbf, seq, off), off)
 
 
+def _uniform_case(rng, n, R, offset0=0, tail=None):
+    """n reads of R bytes (half copied from inserted records) at CSR offsets
+    starting at offset0; `tail` replaces the last read's length."""
+    ins = synth.random_records(rng, 60, 500, 8000, n_prob=0.002)
+    lens = np.full(n, R)
+    if tail is not None:
+        lens[-1] = tail
+    reads = synth.random_records(rng, n, R, R, n_prob=0.003, lower_prob=0.05)
+    body = rng.integers(0, 4, size=offset0 + int(lens.sum()), dtype=np.uint8)
+    seq = np.frombuffer(b"ACGT", dtype=np.uint8)[body]
+    seq[offset0: offset0 + min(n * R, int(lens.sum()))] = reads.seq[: min(n * R, int(lens.sum()))]
+    take = min(ins.seq.size, n * R // 2)
+    seq[offset0: offset0 + take] = ins.seq[:take]
+    off = offset0 + synth.csr(lens)
+    return ins, seq, off
+
+
+@pytest.mark.parametrize("R,n,offset0,tail", [
+    (150, 777, 0, None), (31, 300, 0, None), (160, 129, 0, None), (97, 1, 0, None),
+    (150, 500, 64, None), (150, 500, 7, None), (150, 500, 0, 149), (150, 500, 0, 151),
+    (30, 400, 0, None), (161, 300, 0, None)])
+def test_csr_query_of_uniform_batches(torch, R, n, offset0, tail):
+    """The operating point's CSR query runs a batch whose records are all one
+    length (k <= R <= 160, starting at offset 0) with the one-read-per-strip
+    geometry, and every other batch (a nonzero first offset, one record of
+    another length, records shorter than k or longer than 160) with the CSR
+    one: the answers equal the oracle's either way, and no word outside the
+    answer range is written."""
+    rng = np.random.default_rng(3100 + R + n + offset0)
+    ins, seq, off = _uniform_case(rng, n, R, offset0, tail)
+    sbf = _filter(1 << 18, MAIN, 62)
+    gpu_insert(torch, sbf, ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, MAIN, 1 << 18, 62)
+    want = oracle_answers(F, seq, off, MAIN, 62)
+    got = gpu_query(torch, sbf, seq, off, sentinel=-1)
+    assert_words_equal(got, want, off)
+    lo, hi = int(off[0]) >> 5, (int(off[-1]) + 31) >> 5
+    assert (got[:lo] == 0xFFFFFFFF).all() and (got[hi:] == 0xFFFFFFFF).all()
+    # the host-facing calls: in place (pageable or pinned), staged, no-alloc
+    from minimizer_sharded_bloom_gb300 import _native as N
+    for mode in (0, 1):
+        N.sbf_set_host_mode(sbf.handle, mode)
+        assert_words_equal(sbf.query_host(seq, off), want, off)
+    N.sbf_set_host_mode(sbf.handle, 0)
+    pseq = torch.from_numpy(seq).pin_memory()
+    poff = torch.from_numpy(off.astype(np.int64)).pin_memory()
+    pout = torch.zeros((int(off[-1]) + 31) // 32 + 1, dtype=torch.int32).pin_memory()
+    N.sbf_query_host(sbf.handle, pseq.data_ptr(), poff.data_ptr(), n, pout.data_ptr(), 0)
+    assert_words_equal(pout.numpy().view(np.uint32), want, off)
+    out = np.zeros((int(off[-1]) + 31) // 32 + 1, dtype=np.uint32)
+    N.sbf_query_host_noalloc(sbf.handle, seq.ctypes.data, off.ctypes.data, n, out.ctypes.data, 0)
+    assert_words_equal(out, want, off)
+    sbf.close()
+
+
+def test_concurrent_uniform_and_ragged_queries(torch):
+    """Two streams query one filter at once, one with a uniform batch and one
+    with a ragged batch, many times over: each call's uniformity flag is its
+    own, so both keep answering like the oracle."""
+    rng = np.random.default_rng(3200)
+    ins, useq, uoff = _uniform_case(rng, 3000, 150)
+    rag = synth.random_records(rng, 2000, 60, 240, n_prob=0.003)
+    sbf = _filter(1 << 20, MAIN, 63)
+    gpu_insert(torch, sbf, ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, MAIN, 1 << 20, 63)
+    want_u = oracle_answers(F, useq, uoff, MAIN, 63)
+    want_r = oracle_answers(F, rag.seq, rag.offsets, MAIN, 63)
+    du, dou = to_dev(torch, useq, uoff)
+    dr, dor = to_dev(torch, rag.seq, rag.offsets)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs_u, outs_r = [], []
+    torch.cuda.synchronize()
+    for _ in range(20):
+        ou = torch.zeros((int(uoff[-1]) + 31) // 32 + 1, dtype=torch.int32, device="cuda")
+        orr = torch.zeros((int(rag.offsets[-1]) + 31) // 32 + 1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        sbf.query(du, dou, out=ou, stream=s1)
+        sbf.query(dr, dor, out=orr, stream=s2)
+        outs_u.append(ou)
+        outs_r.append(orr)
+    torch.cuda.synchronize()
+    for ou, orr in zip(outs_u, outs_r):
+        assert_words_equal(ou.cpu().numpy().view(np.uint32), want_u, uoff)
+        assert_words_equal(orr.cpu().numpy().view(np.uint32), want_r, rag.offsets)
+    assert sbf.status() == 0
+    sbf.close()
+
+
 def test_filter_algebra_on_gpu(torch):
     """Order independence, split inserts, idempotence and union, on the GPU
     image (OR is commutative and idempotent)."""
