@@ -263,6 +263,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return false;
 }
 
+// Hint: bring the 128-byte line holding p into L2 (p must be a valid address).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte asynchronous global -> shared copy through L2 only.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -548,9 +553,21 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         }
         // the raw buffer is free again (triplets: after the last frame pass's
         // symbols are formed): start the next tile's copy
+        // A tile without a bulk copy (host memory read in place, the batch's
+        // edges) gets its bytes prefetched into L2 instead, one 128-byte line
+        // per thread and round, clipped to [lo, hi): its direct loads then
+        // hit L2 rather than wait on the link.
         auto next_copy = [&]() {
-            if (tid == 0 && tile + gridDim.x < n_tiles && bulk_ok(tile + gridDim.x))
-                bulk_load(sm.raw, a.seq + (base + (tile + gridDim.x) * tile_pos - OFF), raw_bytes, &sm.raw_bar);
+            const int64_t nt = tile + gridDim.x;
+            if (nt >= n_tiles) return;
+            if (bulk_ok(nt)) {
+                if (tid == 0) bulk_load(sm.raw, a.seq + (base + nt * tile_pos - OFF), raw_bytes, &sm.raw_bar);
+                return;
+            }
+            const int64_t b0 = max(base + nt * tile_pos - OFF, lo);
+            const int64_t b1 = min(base + nt * tile_pos - OFF + (int64_t)raw_bytes, hi);
+            for (int64_t x = (b0 & ~int64_t(127)) + 128 * (int64_t)tid; x < b1; x += 128 * NT)
+                prefetch_l2(a.seq + max(x, b0));
         };
         if constexpr (A != 2) next_copy();
         int prev_res = -1;  // triplets: (A0 - last boundary <= A0) mod 3, -1 if none
