@@ -332,8 +332,8 @@ def main():
     ap.add_argument("--workload", default="out-of-cache", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--host-mode", type=int, default=None, choices=[0, 1],
-                    help="e2e leg: 0 reads host buffers in place, 1 stages chunks (default: the library's)")
+    ap.add_argument("--host-mode", type=int, default=None, choices=[0, 1, 2],
+                    help="e2e leg: 0 the library default, 1 stages chunks, 2 reads host buffers in place")
     ap.add_argument("--host-chunk", type=int, default=None,
                     help="e2e leg: positions per staged chunk (default: the library's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

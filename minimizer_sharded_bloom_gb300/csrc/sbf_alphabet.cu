@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
         }
 
         if (kQuery) {
-            const int64_t w_lo = lo >> 5, w_hi = (hi + 31) >> 5;
+            const int64_t w_lo = lo >> 5, w_hi = min((hi + 31) >> 5, a.out_words_end);
             for (int i = t; i < T::OUTW; i += NT) {
                 const int64_t gw = (t0 >> 5) + i;
                 if (gw >= w_lo && gw < w_hi) a.out[gw] = sm.ans[i];

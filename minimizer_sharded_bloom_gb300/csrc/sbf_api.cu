@@ -147,6 +147,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.device_seq = device_seq ? 1 : 0;
     la.rec_len = 0;
     la.nonuniform = nullptr;
+    la.out_words_end = INT64_MAX;
     return la;
 }
 
@@ -185,8 +186,14 @@ int sbf::launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, i
                   make_args(f, seq, offsets, n, nullptr, device_seq), st);
 }
 
+int sbf::launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream) {
+    if (n == 0) return SBF_OK;
+    return launch_check(f, offsets, n, as_stream(stream));
+}
+
 int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
-                      uint32_t *out_bits, void *stream, bool device_seq, int *flag_word) {
+                      uint32_t *out_bits, void *stream, bool device_seq, int *flag_word,
+                      int64_t out_words_end) {
     if (n == 0) return SBF_OK;
     cudaStream_t st = as_stream(stream);
     // Where the query kernel can run a uniform batch as a dense one, the
@@ -211,6 +218,7 @@ int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offse
     if (rc == SBF_OK) {
         sbf::LaunchArgs la = make_args(f, seq, offsets, n, out_bits, device_seq);
         la.nonuniform = flag;
+        la.out_words_end = out_words_end;
         rc = launch(f->query_kernel, f->grid_query, f->threads_query, la, st);
     }
     if (owned) cudaFreeAsync(flag, st);

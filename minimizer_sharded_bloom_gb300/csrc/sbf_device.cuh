@@ -34,6 +34,8 @@ struct LaunchArgs {
                               // and `offsets` is unused; 0: CSR offsets
     const int *nonuniform;    // CSR queries that may run as dense batches: nonzero when the
                               // offsets check saw records of different lengths (else nullptr)
+    int64_t out_words_end;    // query: answer words at or past this index are not written
+                              // (a chunk of a larger batch cut inside a record); else INT64_MAX
 };
 
 // Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) generic_kernel(LaunchArgs a) {
                            (K[2] & ~__ldg(F + 2)) | (K[3] & ~__ldg(F + 3))) == 0;
             }
             const unsigned bits = __ballot_sync(0xffffffffu, present);
-            if (lane == 0) a.out[w0 >> 5] = bits;
+            if (lane == 0 && (w0 >> 5) < a.out_words_end) a.out[w0 >> 5] = bits;
         } else if (valid) {
             uint64_t *F = a.words + shard * 4;
 #pragma unroll

@@ -2,17 +2,23 @@
 // entry points synchronize; Sec. IV-G "Host FASTX staging": overlap pinned
 // staging and host-to-device copies with kernels on alternating streams).
 //
-// The CSR batch is cut into chunks of output positions [cs, ce) (cs, ce
-// multiples of 32 except at the very end).  A chunk ships the bytes
-// [max(cs, offsets[0]), min(ce + kb - 1, offsets[n])) (kb = bytes of one
-// k-mer) and its records clipped to that range, so every k-mer that starts in
-// [cs, ce) sees exactly its own bytes; k-mers starting at or after ce fall off
-// the clipped end and are invalid in that chunk.  A record clipped at the
-// chunk's start keeps its symbol frame (DNA triplets).  Chunk c runs on slot c & 1 (a stream, device buffers
-// and pinned buffers, all kept in the filter between calls); the host prepares
-// chunk c+1 while the GPU works on chunk c.  Host buffers that are already
-// page-locked are copied from (and to) directly; pageable ones go through the
-// pinned staging buffers.
+// In place: where the device can read (and write) the caller's buffers, one
+// launch reads them directly.  Staged: the CSR batch is cut into chunks of
+// positions [cs, ce) (multiples of 32 except at the very end).  A chunk ends at
+// a record start on a 32-position boundary when one is near ce: its records
+// are whole.  Otherwise it ends at ce itself and ships the bytes up to
+// min(ce + kb - 1, offsets[n]) (kb = bytes of one k-mer) with its last record
+// clipped there; every k-mer starting in [cs, ce) sees exactly its own bytes,
+// and the answer words from ce >> 5 on are left to the next chunk.  A record
+// clipped at a chunk's start keeps its symbol frame (DNA triplets).  The
+// kernels index absolute positions: a chunk's offsets are the caller's, as
+// they are, with both ends clipped, and its staged bytes are addressed through
+// a pointer biased by cs, so the host never rewrites the offsets.  Chunk c
+// runs on slot c & 1 (a stream, device buffers and pinned buffers, all kept in
+// the filter between calls); the host prepares chunk c+1 while the GPU works
+// on chunk c.  Host buffers that are already page-locked are copied from
+// directly; pageable ones go through the pinned staging buffers.  Answers go
+// straight to the caller's buffer where the device can write it.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -62,15 +68,15 @@ cudaError_t grow_pinned(T *&p, int64_t &cap, int64_t need) {
     return e;
 }
 
-cudaError_t prepare(Slot &s, int64_t seq_bytes, int64_t n_off, int64_t out_words, bool stage_seq,
-                    bool stage_out) {
+cudaError_t prepare(Slot &s, int64_t seq_bytes, int64_t n_off, int64_t n_off_host, int64_t out_words,
+                    bool stage_seq, bool stage_out) {
     cudaError_t e = cudaSuccess;
     if (!s.stream) e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = grow_dev(s.d_seq, s.cap_dseq, std::max<int64_t>(seq_bytes, 16));
     if (e == cudaSuccess) e = grow_dev(s.d_off, s.cap_doff, std::max<int64_t>(n_off, 2));
     if (e == cudaSuccess && out_words) e = grow_dev(s.d_out, s.cap_dout, out_words);
     if (e == cudaSuccess && stage_seq) e = grow_pinned(s.h_seq, s.cap_hseq, seq_bytes);
-    if (e == cudaSuccess) e = grow_pinned(s.h_off, s.cap_hoff, std::max<int64_t>(n_off, 2));
+    if (e == cudaSuccess) e = grow_pinned(s.h_off, s.cap_hoff, std::max<int64_t>(n_off_host, 2));
     if (e == cudaSuccess && stage_out) e = grow_pinned(s.h_out, s.cap_hout, out_words);
     return e;
 }
@@ -131,6 +137,10 @@ int run_in_place(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, 
     return 1;
 }
 
+// Records searched back from a nominal chunk end for one that starts on an
+// answer-word boundary.
+constexpr int kEdgeSearch = 64;
+
 // First record r with offsets[r + 1] > g.
 int64_t record_at(const int64_t *off, int64_t n, int64_t g) {
     int64_t lo = 0, hi = n - 1;
@@ -166,34 +176,102 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != f->device)
         return set_error(SBF_ERR_INVALID_ARG, "the filter's device is not current");
-    if (f->host_mode == 0) {
+    // In place (no copies) where the device reads the buffers itself: always
+    // in mode 2; in mode 0 except for a DNA query whose sequence is
+    // page-locked.  That query consumes its input about as fast as the host
+    // link delivers it, and the copy engine moves bytes over the link faster
+    // than the kernel's own loads; its chunks also keep a batch of
+    // equal-length reads dense.  Slower consumers (inserts, bound by their
+    // filter updates; protein and triplet queries) leave the link idle enough
+    // that in place is faster.
+    const bool stage_first = f->host_mode == 1 || (f->host_mode == 0 && query && seq_kind == 1 &&
+                                                   f->alphabet == SBF_ALPHABET_DNA);
+    if (!stage_first) {
         int rc = SBF_OK;
         if (run_in_place(f, seq, off, n, out_bits, user_stream, query, &rc)) return rc;
     }
-    if (int rc = host_check()) return rc;
+    // Staged.  The offsets are checked once, on the device where it reads
+    // them in place (a bad array sets the sticky status: every chunk's kernel
+    // then returns at once), else on the host.
+    const int64_t *off_dev = static_cast<const int64_t *>(device_alias(off, f->device));
+    if (!off_dev)
+        if (int rc = host_check()) return rc;
+    // answers go straight to the caller's buffer where the device can write it
+    uint32_t *out_dev = nullptr;
+    if (query) {
+        if (const void *q = device_alias(out_bits + (lo >> 5), f->device))
+            out_dev = reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(q) -
+                                                   (uintptr_t)(lo >> 5) * sizeof(uint32_t));
+    }
+    const bool off_pinned = host_kind(off) == 1;
     if (!f->stager) f->stager = new Stager;
     Stager &st = *static_cast<Stager *>(f->stager);
 
-    cudaEvent_t ready;
+    // Copies wait for the caller's earlier work (ready); kernels also for the
+    // offsets check (checked), which thus overlaps the first copies.
+    cudaEvent_t ready, checked;
     if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess)
         return set_error(SBF_ERR_CUDA, "cudaEventCreate");
+    if (cudaEventCreateWithFlags(&checked, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(ready);
+        return set_error(SBF_ERR_CUDA, "cudaEventCreate");
+    }
     cudaEventRecord(ready, reinterpret_cast<cudaStream_t>(user_stream));
+    if (off_dev) {
+        if (int rc = sbf::launch_offsets_check(f, off_dev, n, user_stream)) {
+            cudaEventDestroy(ready);
+            cudaEventDestroy(checked);
+            return rc;
+        }
+    }
+    cudaEventRecord(checked, reinterpret_cast<cudaStream_t>(user_stream));
 
+    const int64_t kb = sbf::kmer_bytes(f);
+    const int sb = sbf::symbol_bytes(f->alphabet);
+    // about an eighth of the batch per chunk, so that the first copy, which
+    // nothing overlaps, stays short; at most the filter's chunk setting
+    const int64_t chunk = std::min<int64_t>(
+        f->host_chunk, std::max<int64_t>(((hi - lo) / 8 + 31) & ~int64_t(31), int64_t(1) << 22));
     int rc = SBF_OK;
     int64_t cs = lo & ~int64_t(31);
     for (int64_t c = 0; cs < hi && rc == SBF_OK; ++c) {
-        const int64_t ce = std::min<int64_t>(cs + f->host_chunk, hi);
         const int64_t data_lo = std::max<int64_t>(cs, lo);
-        const int64_t data_hi = std::min<int64_t>(ce + sbf::kmer_bytes(f) - 1, hi);
+        int64_t ce = std::min<int64_t>(cs + chunk, hi);
+        int64_t data_hi = hi;
+        if (ce < hi) {
+            // End the chunk at a record start on an answer-word boundary when
+            // one is near: no record is cut (no k-mer overlap), and the chunk
+            // of a batch of equal-length reads still runs dense.  Else cut at
+            // ce and ship the k - 1 bytes after it.
+            int64_t P = -1;
+            int64_t r = record_at(off, n, ce);
+            for (int t = 0; t < kEdgeSearch && r > 0; ++t, --r) {
+                const int64_t p = off[r];
+                if (p <= data_lo) break;
+                if (p <= ce && (p & 31) == 0) {
+                    P = p;
+                    break;
+                }
+            }
+            if (P > 0) ce = data_hi = P;
+            else data_hi = std::min<int64_t>(ce + kb - 1, hi);
+        }
         const int64_t r0 = record_at(off, n, data_lo);
         const int64_t r1 = record_at(off, n, data_hi - 1) + 1;
+        if (r1 <= r0) {  // only with offsets the check rejects
+            cs = ce;
+            continue;
+        }
         const int64_t n_loc = r1 - r0;
-        // A record clipped at data_lo keeps its symbol frame: its chunk-local
-        // start moves up to its next symbol boundary (triplets; the bytes
-        // skipped start no symbol of the record).
-        const int sb = sbf::symbol_bytes(f->alphabet);
-        const int64_t first_lo = off[r0] < data_lo ? data_lo + (sb - (data_lo - off[r0]) % sb) % sb : data_lo;
-        const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel writes
+        // The chunk's offsets are the caller's, absolute, with both ends
+        // clipped to [data_lo, data_hi]; a record cut at data_lo starts at its
+        // next symbol boundary (DNA triplets keep their codon frame).
+        auto clip = [&](int64_t v) { return std::min<int64_t>(std::max<int64_t>(v, data_lo), data_hi); };
+        const int64_t last = clip(off[r1]);
+        const int64_t next = n_loc >= 2 ? clip(off[r0 + 1]) : last;
+        int64_t first = off[r0] < data_lo ? data_lo + (sb - (data_lo - off[r0]) % sb) % sb : off[r0];
+        first = std::min<int64_t>(clip(first), next);
+        const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel may write
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
         Slot &s = st.slot[c & 1];
         if (s.stream) {
@@ -204,17 +282,14 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             if (s.pend_dst) std::memcpy(s.pend_dst, s.h_out, sizeof(uint32_t) * (size_t)s.pend_words);
             s.pend_dst = nullptr;
         }
-        if (prepare(s, data_hi - cs, n_loc + 1, query ? dev_words : 0, seq_kind == 0,
-                    query && out_kind == 0) != cudaSuccess) {
+        const bool stage_out = query && !out_dev;
+        if (prepare(s, data_hi - cs, n_loc + 1, off_pinned ? 2 : n_loc + 1, stage_out ? dev_words : 0,
+                    seq_kind == 0, stage_out) != cudaSuccess) {
             cudaGetLastError();
             rc = set_error(SBF_ERR_OOM, "staging buffers could not be allocated");
             break;
         }
         cudaStreamWaitEvent(s.stream, ready, 0);
-        for (int64_t r = 0; r <= n_loc; ++r)
-            s.h_off[r] = std::min<int64_t>(std::max<int64_t>(off[r0 + r], data_lo), data_hi) - cs;
-        // (a record that ends before that boundary is left empty)
-        s.h_off[0] = std::min<int64_t>(first_lo - cs, s.h_off[1]);
         const char *src = seq + data_lo;
         char *dst = s.d_seq + (data_lo - cs);
         if (seq_kind == 0) {
@@ -222,29 +297,48 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             src = s.h_seq + (data_lo - cs);
         }
         cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)(data_hi - data_lo), cudaMemcpyHostToDevice, s.stream);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(s.d_off, s.h_off, sizeof(int64_t) * (size_t)(n_loc + 1), cudaMemcpyHostToDevice,
-                                s.stream);
+        const size_t off_bytes = sizeof(int64_t) * (size_t)(n_loc + 1);
+        if (off_pinned) {
+            // the slice straight from the caller's page-locked array, then the two ends
+            s.h_off[0] = first;
+            s.h_off[1] = last;
+            if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, off + r0, off_bytes, cudaMemcpyHostToDevice, s.stream);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, s.h_off, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(s.d_off + n_loc, s.h_off + 1, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+        } else {
+            std::memcpy(s.h_off, off + r0, off_bytes);
+            s.h_off[0] = first;
+            s.h_off[n_loc] = last;
+            if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, s.h_off, off_bytes, cudaMemcpyHostToDevice, s.stream);
+        }
         if (e != cudaSuccess) {
             rc = set_error(SBF_ERR_CUDA, "host-to-device copy: %s", cudaGetErrorString(e));
             break;
         }
+        cudaStreamWaitEvent(s.stream, checked, 0);
+        // the kernel indexes absolute positions: the staged bytes sit at d_seq + (g - cs)
+        const char *k_seq = reinterpret_cast<const char *>(reinterpret_cast<uintptr_t>(s.d_seq) - (uintptr_t)cs);
         if (query) {
-            rc = sbf_query(f, s.d_seq, s.d_off, n_loc, s.d_out, s.stream);
+            uint32_t *k_out = out_dev ? out_dev
+                                      : reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(s.d_out) -
+                                                                     (uintptr_t)(cs >> 5) * sizeof(uint32_t));
+            // a chunk cut inside a record leaves the words from ce on to the next chunk
+            rc = sbf::launch_query(f, k_seq, s.d_off, n_loc, k_out, s.stream, true, nullptr,
+                                   ce < hi ? (ce >> 5) : INT64_MAX);
             if (rc != SBF_OK) break;
-            uint32_t *final_dst = out_bits + (cs >> 5);
-            uint32_t *land = out_kind == 1 ? final_dst : s.h_out;
-            e = cudaMemcpyAsync(land, s.d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost, s.stream);
-            if (e != cudaSuccess) {
-                rc = set_error(SBF_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
-                break;
-            }
-            if (out_kind == 0) {
-                s.pend_dst = final_dst;
+            if (stage_out) {
+                e = cudaMemcpyAsync(s.h_out, s.d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost,
+                                    s.stream);
+                if (e != cudaSuccess) {
+                    rc = set_error(SBF_ERR_CUDA, "device-to-host copy: %s", cudaGetErrorString(e));
+                    break;
+                }
+                s.pend_dst = out_bits + (cs >> 5);
                 s.pend_words = words;
             }
         } else {
-            rc = sbf_insert(f, s.d_seq, s.d_off, n_loc, s.stream);
+            rc = sbf::launch_insert(f, k_seq, s.d_off, n_loc, s.stream, true);
             if (rc != SBF_OK) break;
         }
         cs = ce;
@@ -257,10 +351,8 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         s.pend_dst = nullptr;
     }
     cudaEventDestroy(ready);
-    if (rc == SBF_OK) {
-        // the device check of the chunk offsets could only have failed if the host check missed it
-        rc = sbf_get_status(f, nullptr);
-    }
+    cudaEventDestroy(checked);
+    if (rc == SBF_OK) rc = sbf_get_status(f, user_stream);
     return rc;
 }
 
@@ -285,7 +377,7 @@ void sbf::destroy_stager(void *p) {
 extern "C" {
 
 int sbf_set_host_mode(sbf_filter *f, int mode) {
-    if (!f || mode < 0 || mode > 1) return sbf::set_error(SBF_ERR_INVALID_ARG, "sbf_set_host_mode: mode is 0 or 1");
+    if (!f || mode < 0 || mode > 2) return sbf::set_error(SBF_ERR_INVALID_ARG, "sbf_set_host_mode: mode is 0, 1 or 2");
     f->host_mode = mode;
     return SBF_OK;
 }

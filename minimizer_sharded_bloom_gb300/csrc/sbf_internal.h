@@ -27,7 +27,7 @@ struct sbf_filter {
     int grid_check = 0;
     bool specialized = false;
     void *stager = nullptr;     // host-facing staging buffers, created on first use
-    int64_t host_chunk = int64_t(1) << 27;  // host-facing chunk, in positions
+    int64_t host_chunk = int64_t(1) << 26;  // host-facing chunk, in positions
     int host_mode = 0;          // 0: read host buffers in place when possible; 1: always stage
 };
 
@@ -45,6 +45,11 @@ int launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_
                   bool device_seq);
 // flag_word: a device int the call may use to detect a uniform batch (the
 // no-alloc path passes one of its own); nullptr: allocated per call.
+// out_words_end: answer words at or past this index are left unwritten.
 int launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
-                 uint32_t *out_bits, void *stream, bool device_seq, int *flag_word = nullptr);
+                 uint32_t *out_bits, void *stream, bool device_seq, int *flag_word = nullptr,
+                 int64_t out_words_end = INT64_MAX);
+// The device check of an offsets array (device-accessible) alone; a bad array
+// sets the sticky status, which every later launch of the filter honours.
+int launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream);
 }  // namespace sbf

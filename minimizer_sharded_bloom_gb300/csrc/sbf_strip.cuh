@@ -382,11 +382,12 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
     // dense batches: record r is bytes [r rlen, (r + 1) rlen), a tile holds NT
     // records; the geometry below is runtime there and the constants otherwise.
     // A CSR batch runs dense too when the offsets check found every record of
-    // one length rlen (K <= rlen <= D) and the batch starts at offset 0.
+    // one length rlen (K <= rlen <= D) and its first offset is a multiple of 32
+    // (tiles then start on answer-word boundaries, at records).
     int rlen = D > 0 ? (int)a.rec_len : 0;
     if (D > 0 && rlen == 0 && a.nonuniform != nullptr && *a.nonuniform == 0) {
         const int64_t o0 = a.offsets[0], len0 = a.offsets[1] - o0;
-        if (o0 == 0 && len0 >= K && len0 <= D) rlen = (int)len0;
+        if ((o0 & 31) == 0 && len0 >= K && len0 <= D) rlen = (int)len0;
     }
     const bool dense = D > 0 && rlen > 0;
     const int tile_pos = dense ? NT * rlen : BT;               // positions (bytes) per tile
@@ -880,7 +881,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         __syncthreads();
         }  // frame passes
         if (kQuery) {
-            const int64_t w_lo = lo >> 5, w_hi = (hi + 31) >> 5;
+            const int64_t w_lo = lo >> 5, w_hi = min((hi + 31) >> 5, a.out_words_end);
             for (int w = tid; w < (dense ? tile_words : C::OUT_WORDS); w += NT) {
                 const int64_t gw = (T0 >> 5) + w;
                 if (gw >= w_lo && gw < w_hi) a.out[gw] = sm.outw[w];

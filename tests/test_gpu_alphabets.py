@@ -161,12 +161,12 @@ def test_create_rejects_k_beyond_packing(torch, alphabet):
         SuperBloomFilter(1 << 10, k=5, m=2, s=2, H=2, alphabet="rna")
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("alphabet,params", [("protein", PROTEIN), ("dna_triplet", TRIPLET)])
 def test_host_entry_points(torch, alphabet, params, mode):
-    """sbf_insert_host / sbf_query_host in place (mode 0) and staged in chunks
-    of 4096 positions (mode 1): chunk edges cut records at every phase of
-    their codon frame, which each chunk must keep."""
+    """sbf_insert_host / sbf_query_host in place (modes 0 and 2) and staged in
+    chunks of 4096 positions (mode 1): chunk edges cut records at every phase
+    of their codon frame, which each chunk must keep."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(73)
     ins = _records(rng, alphabet, 30, 0, 5000, 1)

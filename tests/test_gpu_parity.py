@@ -180,12 +180,12 @@ def test_bad_offsets_set_the_status(torch):
     assert_images_equal(sbf.to_numpy(), oracle_image(seq, good, MAIN, 1 << 14, 4))
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_host_calls_report_bad_offsets(torch, mode):
     """Host-facing insert/query with decreasing offsets fail with
-    SBF_ERR_BAD_OFFSETS (found by the device check when the buffers are read
-    in place, mode 0; by the host before chunking, mode 1), change nothing,
-    leave the status clear, and the next good call works."""
+    SBF_ERR_BAD_OFFSETS (found by the device check, on the offsets read in
+    place, before any chunk runs), change nothing, leave the status clear,
+    and the next good call works."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(14)
     seq = synth.uniform_bases(rng, 4000)
@@ -202,6 +202,15 @@ def test_host_calls_report_bad_offsets(torch, mode):
     with pytest.raises(N.SBFError) as err:
         sbf.query_host(seq, bad, out=out)
     assert err.value.code == N.SBF_ERR_BAD_OFFSETS
+    assert sbf.status() == 0
+    # page-locked buffers (mode 0 stages a page-locked query): nothing written
+    pseq = torch.from_numpy(seq).pin_memory()
+    pbad = torch.from_numpy(bad).pin_memory()
+    pout = torch.full((4000 // 32 + 2,), -1, dtype=torch.int32).pin_memory()
+    with pytest.raises(N.SBFError) as err:
+        N.sbf_query_host(sbf.handle, pseq.data_ptr(), pbad.data_ptr(), 3, pout.data_ptr(), 0)
+    assert err.value.code == N.SBF_ERR_BAD_OFFSETS
+    assert (pout.numpy() == -1).all()
     assert sbf.status() == 0
     sbf.insert_host(seq, good)
     F = oracle_image(seq, good, MAIN, 1 << 14, 4)
@@ -301,6 +310,51 @@ def test_csr_query_of_uniform_batches(torch, R, n, offset0, tail):
     sbf.close()
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("pinned", [False, True])
+@pytest.mark.parametrize("case", ["reads", "long", "mixed"])
+def test_host_query_chunk_edges(torch, case, pinned, mode):
+    """Host-facing queries cut into chunks of 4096 positions: a batch of
+    150 bp reads (every chunk ends at a read that starts on a 32-position
+    boundary and runs dense), records longer than a chunk (chunks cut inside
+    records: each leaves the answer words from its cut on to the next), and a
+    mix with empty records.  Answers equal the oracle's, and no word outside
+    the answer range is written."""
+    from minimizer_sharded_bloom_gb300 import _native as N
+    rng = np.random.default_rng({"reads": 3300, "long": 3301, "mixed": 3302}[case])
+    ins = synth.random_records(rng, 40, 500, 6000, n_prob=0.002)
+    if case == "reads":
+        q = synth.random_records(rng, 400, 150, 150, n_prob=0.003)
+    elif case == "long":
+        q = synth.random_records(rng, 6, 5000, 13000, n_prob=0.002)
+    else:
+        q = synth.random_records(rng, 120, 0, 3000, n_prob=0.002)
+    seq = q.seq.copy()
+    take = min(ins.seq.size, seq.size // 2)
+    seq[:take] = ins.seq[:take]
+    off = q.offsets.copy()
+    sbf = _filter(1 << 16, MAIN, 64)
+    gpu_insert(torch, sbf, ins.seq, ins.offsets)
+    F = oracle_image(ins.seq, ins.offsets, MAIN, 1 << 16, 64)
+    want = oracle_answers(F, seq, off, MAIN, 64)
+    N.sbf_set_host_chunk(sbf.handle, 4096)
+    N.sbf_set_host_mode(sbf.handle, mode)
+    words = (int(off[-1]) + 31) // 32
+    if pinned:
+        ks = torch.from_numpy(seq).pin_memory()
+        ko = torch.from_numpy(off).pin_memory()
+        kt = torch.full((words + 3,), -1, dtype=torch.int32).pin_memory()
+        N.sbf_query_host(sbf.handle, ks.data_ptr(), ko.data_ptr(), q.n_records, kt.data_ptr(), 0)
+        got = kt.numpy().view(np.uint32)
+    else:
+        got = np.full(words + 3, 0xFFFFFFFF, dtype=np.uint32)
+        N.sbf_query_host(sbf.handle, seq.ctypes.data, off.ctypes.data, q.n_records, got.ctypes.data, 0)
+    assert_words_equal(got, want, off)
+    assert (got[words:] == 0xFFFFFFFF).all()
+    assert sbf.status() == 0
+    sbf.close()
+
+
 def test_concurrent_uniform_and_ragged_queries(torch):
     """Two streams query one filter at once, one with a uniform batch and one
     with a ragged batch, many times over: each call's uniformity flag is its
@@ -372,14 +426,15 @@ def test_copy_load_clear(torch):
     assert not s2.to_numpy().any()
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("pinned", [False, True])
 @pytest.mark.parametrize("params", [MAIN, dict(k=25, m=11, s=20, H=3)])
 def test_host_entry_points(torch, pinned, params, mode):
     """sbf_insert_host / sbf_query_host, reading the host buffers in place
-    (mode 0, when the device can) or staged in chunks of 4096 positions so that
-    records and k-mers straddle chunk edges (mode 1), with pageable and pinned
-    host buffers, equal the oracle."""
+    (mode 2, and mode 0 except a pinned DNA query) or staged in chunks of 4096
+    positions so that chunks end at records or cut them (mode 1, and mode 0
+    for a pinned DNA query), with pageable and pinned host buffers, equal the
+    oracle."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(13)
     ins = synth.random_records(rng, 30, 0, 2500, n_prob=0.002)
