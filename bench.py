@@ -681,7 +681,8 @@ def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
         N.sbf_query_host(sbf.handle, h_q.data_ptr(), h_qo.data_ptr(), qry.n_records,
                          h_out.data_ptr(), 0)
 
-    one()
+    for _ in range(2):  # the first calls size the staging buffers
+        one()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()

@@ -138,14 +138,13 @@ int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int6
 /* Host-facing insert: seq and offsets are HOST pointers (pageable or
  * pinned), same layout as sbf_insert.  Returns when the filter holds every
  * k-mer; the work is ordered after earlier work on `stream` (may be NULL).
- * When the device can access the buffers in place -- page-locked memory, or
- * pageable memory on a device with pageable-memory access through the host
- * page tables (Grace systems over NVLink-C2C) -- the kernels read them
- * directly, with no copies.  Otherwise (or after sbf_set_host_mode(f, 1)) the
- * records are staged to the device in chunks on two alternating streams,
- * overlapping copies with kernels (Sec. IV-G, host FASTX staging):
- * page-locked buffers are copied from directly, pageable ones through pinned
- * staging buffers.  Chunks end at record starts where possible; a record
+ * A page-locked sequence is staged (below).  A pageable one is read in place
+ * when the device can access it -- pageable-memory access through the host
+ * page tables (Grace systems over NVLink-C2C) -- with no copies.  Otherwise
+ * (or after sbf_set_host_mode(f, 1)) the records are staged to the device in
+ * chunks on four rotating streams, overlapping copies with kernels (Sec. IV-G,
+ * host FASTX staging): page-locked buffers are copied from directly, pageable
+ * ones through pinned staging buffers.  Chunks end at record starts where possible; a record
  * longer than a chunk is cut, with the k-1 bytes of overlap its k-mers need.
  * The offsets are checked once before any chunk runs: on the device where it
  * can read them, else on the host. */
@@ -154,11 +153,9 @@ int sbf_insert_host(sbf_filter *f, const char *seq, const int64_t *offsets, int6
 
 /* Host-facing query: seq/offsets/out_bits are HOST pointers, same layout and
  * output contract as sbf_query.  Returns when out_bits is complete.  Reads and
- * writes the host buffers in place or stages them, as sbf_insert_host, except
- * that in mode 0 a page-locked sequence is staged on a DNA filter (the copy
- * engine moves it over the host link faster than the kernel's own loads, and
- * that query consumes input about as fast as the link delivers it).  Staged answers
- * are written straight into out_bits where the device can write it.  With
+ * writes the host buffers in place or stages them, as sbf_insert_host.
+ * Staged answers are written straight into out_bits where the device can
+ * write it.  With
  * malformed offsets (SBF_ERR_BAD_OFFSETS) no answer word is written, except
  * when out_bits is pageable memory the device cannot access: the staged
  * chunks' words may then hold anything. */
@@ -184,16 +181,18 @@ int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets,
 int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                            uint32_t *out_bits, void *stream);
 
-/* Host-facing access mode: 0 (default) reads host buffers in place when the
- * device can, except a DNA query's page-locked sequence, and stages the rest;
- * 1 always stages; 2 reads in place whenever the device can. */
+/* Host-facing access mode: 0 (default) stages a page-locked sequence (the copy
+ * engine moves it over the host link faster than kernel loads) and reads a
+ * pageable one in place when the device can, else stages it; 1 always stages;
+ * 2 reads in place whenever the device can. */
 int sbf_set_host_mode(sbf_filter *f, int mode);
 
 /* Largest chunk of the staged host-facing calls, in sequence positions (default 2^26;
  * rounded down to a multiple of 32; at least 32).  A call cuts its batch into
- * chunks of about an eighth of it, at least 2^22 positions and at most this
- * setting.  Smaller chunks overlap copies and kernels at a finer grain and
- * need smaller staging buffers. */
+ * chunks of up to about an eighth of it, at least 2^22 positions and at most this
+ * setting; the first chunks are smaller (from 2^22 positions, doubling).
+ * Smaller chunks overlap copies and kernels at a finer grain and need smaller
+ * staging buffers. */
 int sbf_set_host_chunk(sbf_filter *f, int64_t positions);
 
 /* ---- FASTA / FASTQ input (Sec. IV-A: streamed FASTA/FASTQ with transparent

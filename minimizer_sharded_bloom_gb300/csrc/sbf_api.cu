@@ -343,6 +343,13 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
                 if (cudaMemPoolCreate(&f->flag_pool, &props) == cudaSuccess) {
                     uint64_t keep = UINT64_MAX;
                     cudaMemPoolSetAttribute(f->flag_pool, cudaMemPoolAttrReleaseThreshold, &keep);
+                    // map the pool's memory now, not under the first queries
+                    void *warm = nullptr;
+                    if (cudaMallocFromPoolAsync(&warm, size_t(1) << 20, f->flag_pool, 0) == cudaSuccess) {
+                        cudaFreeAsync(warm, 0);
+                        cudaStreamSynchronize(0);
+                    }
+                    cudaGetLastError();
                     f->query_detects_dense = true;
                 } else {
                     cudaGetLastError();

@@ -14,7 +14,7 @@
 // kernels index absolute positions: a chunk's offsets are the caller's, as
 // they are, with both ends clipped, and its staged bytes are addressed through
 // a pointer biased by cs, so the host never rewrites the offsets.  Chunk c
-// runs on slot c & 1 (a stream, device buffers and pinned buffers, all kept in
+// runs on slot c mod 4 (a stream, device buffers and pinned buffers, all kept in
 // the filter between calls); the host prepares chunk c+1 while the GPU works
 // on chunk c.  Host buffers that are already page-locked are copied from
 // directly; pageable ones go through the pinned staging buffers.  Answers go
@@ -33,6 +33,7 @@ struct Slot {
     char *d_seq = nullptr;
     int64_t *d_off = nullptr;
     uint32_t *d_out = nullptr;
+    int *d_flag = nullptr;      // the query's uniform-batch flag word (one per slot: no allocation per chunk)
     char *h_seq = nullptr;      // pinned staging for pageable sequence input
     int64_t *h_off = nullptr;   // pinned chunk-local offsets
     uint32_t *h_out = nullptr;  // pinned staging for pageable output
@@ -43,7 +44,9 @@ struct Slot {
 };
 
 struct Stager {
-    Slot slot[2];
+    // four slots: a chunk's copy waits only for the chunk four back, which
+    // leaves the copy engine slack when copies and kernels take about as long
+    Slot slot[4];
 };
 
 template <typename T>
@@ -72,6 +75,7 @@ cudaError_t prepare(Slot &s, int64_t seq_bytes, int64_t n_off, int64_t n_off_hos
                     bool stage_seq, bool stage_out) {
     cudaError_t e = cudaSuccess;
     if (!s.stream) e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess && !s.d_flag) e = cudaMalloc(reinterpret_cast<void **>(&s.d_flag), sizeof(int));
     if (e == cudaSuccess) e = grow_dev(s.d_seq, s.cap_dseq, std::max<int64_t>(seq_bytes, 16));
     if (e == cudaSuccess) e = grow_dev(s.d_off, s.cap_doff, std::max<int64_t>(n_off, 2));
     if (e == cudaSuccess && out_words) e = grow_dev(s.d_out, s.cap_dout, out_words);
@@ -177,15 +181,11 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     if (cudaGetDevice(&dev) != cudaSuccess || dev != f->device)
         return set_error(SBF_ERR_INVALID_ARG, "the filter's device is not current");
     // In place (no copies) where the device reads the buffers itself: always
-    // in mode 2; in mode 0 except for a DNA query whose sequence is
-    // page-locked.  That query consumes its input about as fast as the host
-    // link delivers it, and the copy engine moves bytes over the link faster
-    // than the kernel's own loads; its chunks also keep a batch of
-    // equal-length reads dense.  Slower consumers (inserts, bound by their
-    // filter updates; protein and triplet queries) leave the link idle enough
-    // that in place is faster.
-    const bool stage_first = f->host_mode == 1 || (f->host_mode == 0 && query && seq_kind == 1 &&
-                                                   f->alphabet == SBF_ALPHABET_DNA);
+    // in mode 2; in mode 0 only for a pageable sequence.  A page-locked one is
+    // staged: the copy engine moves it over the host link faster than the
+    // kernel's own loads, and the chunks keep a batch of equal-length reads
+    // dense.  (A pageable sequence would need a host copy into pinned memory.)
+    const bool stage_first = f->host_mode == 1 || (f->host_mode == 0 && seq_kind == 1);
     if (!stage_first) {
         int rc = SBF_OK;
         if (run_in_place(f, seq, off, n, out_bits, user_stream, query, &rc)) return rc;
@@ -228,10 +228,12 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
 
     const int64_t kb = sbf::kmer_bytes(f);
     const int sb = sbf::symbol_bytes(f->alphabet);
-    // about an eighth of the batch per chunk, so that the first copy, which
-    // nothing overlaps, stays short; at most the filter's chunk setting
-    const int64_t chunk = std::min<int64_t>(
+    // Chunks start at 2^22 positions and double up to about an eighth of the
+    // batch (at most the filter's chunk setting): the first copy, which no
+    // kernel overlaps, stays short, and later ones are large.
+    const int64_t chunk_max = std::min<int64_t>(
         f->host_chunk, std::max<int64_t>(((hi - lo) / 8 + 31) & ~int64_t(31), int64_t(1) << 22));
+    int64_t chunk = std::min<int64_t>(chunk_max, int64_t(1) << 22);
     int rc = SBF_OK;
     int64_t cs = lo & ~int64_t(31);
     for (int64_t c = 0; cs < hi && rc == SBF_OK; ++c) {
@@ -273,7 +275,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         first = std::min<int64_t>(clip(first), next);
         const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel may write
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
-        Slot &s = st.slot[c & 1];
+        Slot &s = st.slot[c % 4];
         if (s.stream) {
             if (cudaStreamSynchronize(s.stream) != cudaSuccess) {
                 rc = set_error(SBF_ERR_CUDA, "staging stream failed");
@@ -283,8 +285,12 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             s.pend_dst = nullptr;
         }
         const bool stage_out = query && !out_dev;
-        if (prepare(s, data_hi - cs, n_loc + 1, off_pinned ? 2 : n_loc + 1, stage_out ? dev_words : 0,
-                    seq_kind == 0, stage_out) != cudaSuccess) {
+        // sized for the largest chunk at once: growing a buffer mid-call would
+        // free it, which waits for the whole device
+        const int64_t max_bytes = std::max<int64_t>(data_hi - cs, chunk_max + kb);
+        if (prepare(s, max_bytes, n_loc + 1, off_pinned ? 2 : n_loc + 1,
+                    stage_out ? std::max<int64_t>(dev_words, (max_bytes + 31) / 32 + 1) : 0, seq_kind == 0,
+                    stage_out) != cudaSuccess) {
             cudaGetLastError();
             rc = set_error(SBF_ERR_OOM, "staging buffers could not be allocated");
             break;
@@ -324,7 +330,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
                                       : reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(s.d_out) -
                                                                      (uintptr_t)(cs >> 5) * sizeof(uint32_t));
             // a chunk cut inside a record leaves the words from ce on to the next chunk
-            rc = sbf::launch_query(f, k_seq, s.d_off, n_loc, k_out, s.stream, true, nullptr,
+            rc = sbf::launch_query(f, k_seq, s.d_off, n_loc, k_out, s.stream, true, s.d_flag,
                                    ce < hi ? (ce >> 5) : INT64_MAX);
             if (rc != SBF_OK) break;
             if (stage_out) {
@@ -342,6 +348,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             if (rc != SBF_OK) break;
         }
         cs = ce;
+        chunk = std::min<int64_t>(2 * chunk, chunk_max);
     }
     for (Slot &s : st.slot) {
         if (!s.stream) continue;
@@ -366,6 +373,7 @@ void sbf::destroy_stager(void *p) {
         cudaFree(s.d_seq);
         cudaFree(s.d_off);
         cudaFree(s.d_out);
+        cudaFree(s.d_flag);
         cudaFreeHost(s.h_seq);
         cudaFreeHost(s.h_off);
         cudaFreeHost(s.h_out);

@@ -162,11 +162,13 @@ def test_create_rejects_k_beyond_packing(torch, alphabet):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("pinned", [False, True])
 @pytest.mark.parametrize("alphabet,params", [("protein", PROTEIN), ("dna_triplet", TRIPLET)])
-def test_host_entry_points(torch, alphabet, params, mode):
-    """sbf_insert_host / sbf_query_host in place (modes 0 and 2) and staged in
-    chunks of 4096 positions (mode 1): chunk edges cut records at every phase
-    of their codon frame, which each chunk must keep."""
+def test_host_entry_points(torch, alphabet, params, pinned, mode):
+    """sbf_insert_host / sbf_query_host in place (mode 2, and mode 0 for
+    pageable buffers) and staged in chunks of 4096 positions (mode 1, and
+    mode 0 for pinned buffers): chunk edges cut records at every phase of
+    their codon frame, which each chunk must keep."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(73)
     ins = _records(rng, alphabet, 30, 0, 5000, 1)
@@ -174,10 +176,19 @@ def test_host_entry_points(torch, alphabet, params, mode):
     sbf = _filter(1 << 16, params, 21, alphabet)
     N.sbf_set_host_chunk(sbf.handle, 4096)
     N.sbf_set_host_mode(sbf.handle, mode)
-    sbf.insert_host(ins.seq, ins.offsets)
+    keep = []
+
+    def host(a):
+        if not pinned:
+            return np.ascontiguousarray(a)
+        t = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        keep.append(t)
+        return t.numpy()
+    sbf.insert_host(host(ins.seq), host(ins.offsets))
     F = oracle_image(ins.seq, ins.offsets, params, 1 << 16, 21, alphabet=alphabet)
     assert_images_equal(sbf.to_numpy(), F)
-    out = sbf.query_host(qry.seq, qry.offsets)
+    out = host(np.zeros((int(qry.offsets[-1]) + 31) // 32 + 1, dtype=np.uint32))
+    sbf.query_host(host(qry.seq), host(qry.offsets), out=out)
     assert_words_equal(out, oracle_answers(F, qry.seq, qry.offsets, params, 21, alphabet=alphabet),
                        qry.offsets)
 

@@ -203,7 +203,7 @@ def test_host_calls_report_bad_offsets(torch, mode):
         sbf.query_host(seq, bad, out=out)
     assert err.value.code == N.SBF_ERR_BAD_OFFSETS
     assert sbf.status() == 0
-    # page-locked buffers (mode 0 stages a page-locked query): nothing written
+    # page-locked buffers (staged in mode 0): nothing written
     pseq = torch.from_numpy(seq).pin_memory()
     pbad = torch.from_numpy(bad).pin_memory()
     pout = torch.full((4000 // 32 + 2,), -1, dtype=torch.int32).pin_memory()
@@ -431,9 +431,9 @@ def test_copy_load_clear(torch):
 @pytest.mark.parametrize("params", [MAIN, dict(k=25, m=11, s=20, H=3)])
 def test_host_entry_points(torch, pinned, params, mode):
     """sbf_insert_host / sbf_query_host, reading the host buffers in place
-    (mode 2, and mode 0 except a pinned DNA query) or staged in chunks of 4096
+    (mode 2, and mode 0 for pageable buffers) or staged in chunks of 4096
     positions so that chunks end at records or cut them (mode 1, and mode 0
-    for a pinned DNA query), with pageable and pinned host buffers, equal the
+    for pinned buffers), with pageable and pinned host buffers, equal the
     oracle."""
     from minimizer_sharded_bloom_gb300 import _native as N
     rng = np.random.default_rng(13)
