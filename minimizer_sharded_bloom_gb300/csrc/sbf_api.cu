@@ -178,22 +178,24 @@ int sbf::set_error(int code, const char *fmt, ...) {
 }
 
 int sbf::launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream,
-                       bool device_seq) {
+                       bool device_seq, bool run_check) {
     if (n == 0) return SBF_OK;
     cudaStream_t st = as_stream(stream);
-    if (int rc = launch_check(f, offsets, n, st)) return rc;
+    if (run_check)
+        if (int rc = launch_check(f, offsets, n, st)) return rc;
     return launch(f->insert_kernel, f->grid_insert, f->threads,
                   make_args(f, seq, offsets, n, nullptr, device_seq), st);
 }
 
-int sbf::launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream) {
+int sbf::launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream,
+                              int *nonuniform) {
     if (n == 0) return SBF_OK;
-    return launch_check(f, offsets, n, as_stream(stream));
+    return launch_check(f, offsets, n, as_stream(stream), nonuniform);
 }
 
 int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                       uint32_t *out_bits, void *stream, bool device_seq, int *flag_word,
-                      int64_t out_words_end) {
+                      int64_t out_words_end, bool run_check) {
     if (n == 0) return SBF_OK;
     cudaStream_t st = as_stream(stream);
     // Where the query kernel can run a uniform batch as a dense one, the
@@ -203,7 +205,10 @@ int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offse
     // the kernel keeps the CSR geometry, which is correct for every batch.
     int *flag = nullptr;
     bool owned = false;
-    if (f->query_detects_dense) {
+    if (!run_check) {
+        // offsets checked (and the flag set) by the caller beforehand
+        flag = f->query_detects_dense ? flag_word : nullptr;
+    } else if (f->query_detects_dense) {
         if (flag_word) {
             flag = flag_word;
         } else if (cudaMallocFromPoolAsync(reinterpret_cast<void **>(&flag), sizeof(int), f->flag_pool, st) ==
@@ -214,7 +219,7 @@ int sbf::launch_query(const sbf_filter *f, const char *seq, const int64_t *offse
             flag = nullptr;
         }
     }
-    int rc = launch_check(f, offsets, n, st, flag);
+    int rc = run_check ? launch_check(f, offsets, n, st, flag) : SBF_OK;
     if (rc == SBF_OK) {
         sbf::LaunchArgs la = make_args(f, seq, offsets, n, out_bits, device_seq);
         la.nonuniform = flag;

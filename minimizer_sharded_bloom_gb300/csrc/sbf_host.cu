@@ -47,7 +47,13 @@ struct Stager {
     // four slots: a chunk's copy waits only for the chunk four back, which
     // leaves the copy engine slack when copies and kernels take about as long
     Slot slot[4];
+    int64_t *d_all_off = nullptr;  // the whole offsets array of a call, on the device
+    int64_t cap_all_off = 0;
+    int *d_call_flag = nullptr;    // its uniformity flag (from the one check of the call)
 };
+
+// Offsets arrays up to this many entries (256 MiB) go to the device whole.
+constexpr int64_t kAllOffMax = int64_t(1) << 25;
 
 template <typename T>
 cudaError_t grow_dev(T *&p, int64_t &cap, int64_t need) {
@@ -194,8 +200,6 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     // them in place (a bad array sets the sticky status: every chunk's kernel
     // then returns at once), else on the host.
     const int64_t *off_dev = static_cast<const int64_t *>(device_alias(off, f->device));
-    if (!off_dev)
-        if (int rc = host_check()) return rc;
     // answers go straight to the caller's buffer where the device can write it
     uint32_t *out_dev = nullptr;
     if (query) {
@@ -206,6 +210,23 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     const bool off_pinned = host_kind(off) == 1;
     if (!f->stager) f->stager = new Stager;
     Stager &st = *static_cast<Stager *>(f->stager);
+    // For a query, where it fits, the whole offsets array crosses the host
+    // link once: one copy to the device, one check there (which also finds
+    // whether every record has one length), and chunks whose two ends are
+    // record starts index that copy directly, with no check of their own.
+    // (Measured on the 1 Gbp insert this was slower, 7.3 against 6.1 ms, so
+    // an insert ships each chunk's slice and checks it.)
+    bool all_off = query && n + 1 <= kAllOffMax;
+    if (all_off) {
+        cudaError_t e = grow_dev(st.d_all_off, st.cap_all_off, n + 1);
+        if (e == cudaSuccess && !st.d_call_flag) e = cudaMalloc(reinterpret_cast<void **>(&st.d_call_flag), sizeof(int));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            all_off = false;
+        }
+    }
+    if (!all_off && !off_dev)
+        if (int rc = host_check()) return rc;
 
     // Copies wait for the caller's earlier work (ready); kernels also for the
     // offsets check (checked), which thus overlaps the first copies.
@@ -217,12 +238,20 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         return set_error(SBF_ERR_CUDA, "cudaEventCreate");
     }
     cudaEventRecord(ready, reinterpret_cast<cudaStream_t>(user_stream));
-    if (off_dev) {
-        if (int rc = sbf::launch_offsets_check(f, off_dev, n, user_stream)) {
-            cudaEventDestroy(ready);
-            cudaEventDestroy(checked);
-            return rc;
-        }
+    int *call_flag = query && f->query_detects_dense ? st.d_call_flag : nullptr;
+    int crc = SBF_OK;
+    if (all_off) {
+        cudaError_t e = cudaMemcpyAsync(st.d_all_off, off, sizeof(int64_t) * (size_t)(n + 1), cudaMemcpyHostToDevice,
+                                        reinterpret_cast<cudaStream_t>(user_stream));
+        crc = e == cudaSuccess ? sbf::launch_offsets_check(f, st.d_all_off, n, user_stream, call_flag)
+                               : set_error(SBF_ERR_CUDA, "offsets copy: %s", cudaGetErrorString(e));
+    } else if (off_dev) {
+        crc = sbf::launch_offsets_check(f, off_dev, n, user_stream);
+    }
+    if (crc != SBF_OK) {
+        cudaEventDestroy(ready);
+        cudaEventDestroy(checked);
+        return crc;
     }
     cudaEventRecord(checked, reinterpret_cast<cudaStream_t>(user_stream));
 
@@ -235,10 +264,18 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         f->host_chunk, std::max<int64_t>(((hi - lo) / 8 + 31) & ~int64_t(31), int64_t(1) << 22));
     int64_t chunk = std::min<int64_t>(chunk_max, int64_t(1) << 22);
     int rc = SBF_OK;
+    // ... and for a query they shrink again towards the end (at most half of
+    // what is left), so that its last kernel, which no copy overlaps, is
+    // short too.  (An insert's kernels take longer than its copies, and
+    // small launches of its random updates cost throughput.)
     int64_t cs = lo & ~int64_t(31);
     for (int64_t c = 0; cs < hi && rc == SBF_OK; ++c) {
         const int64_t data_lo = std::max<int64_t>(cs, lo);
-        int64_t ce = std::min<int64_t>(cs + chunk, hi);
+        const int64_t cur =
+            query ? std::min<int64_t>(chunk, std::max<int64_t>(((hi - cs) / 2 + 31) & ~int64_t(31),
+                                                               std::min<int64_t>(chunk, int64_t(1) << 22)))
+                  : chunk;
+        int64_t ce = std::min<int64_t>(cs + cur, hi);
         int64_t data_hi = hi;
         if (ce < hi) {
             // End the chunk at a record start on an answer-word boundary when
@@ -304,7 +341,24 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         }
         cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)(data_hi - data_lo), cudaMemcpyHostToDevice, s.stream);
         const size_t off_bytes = sizeof(int64_t) * (size_t)(n_loc + 1);
-        if (off_pinned) {
+        // both ends at record starts: the caller's slice as it is
+        const bool whole = first == off[r0] && last == off[r1];
+        const int64_t *k_off = s.d_off;
+        if (all_off) {
+            // from the device copy of the whole array (written before `checked`)
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s.stream, checked, 0);
+            if (whole) {
+                k_off = st.d_all_off + r0;
+            } else {
+                s.h_off[0] = first;
+                s.h_off[1] = last;
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(s.d_off, st.d_all_off + r0, off_bytes, cudaMemcpyDeviceToDevice, s.stream);
+                if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, s.h_off, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(s.d_off + n_loc, s.h_off + 1, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+            }
+        } else if (off_pinned) {
             // the slice straight from the caller's page-locked array, then the two ends
             s.h_off[0] = first;
             s.h_off[1] = last;
@@ -329,9 +383,15 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             uint32_t *k_out = out_dev ? out_dev
                                       : reinterpret_cast<uint32_t *>(reinterpret_cast<uintptr_t>(s.d_out) -
                                                                      (uintptr_t)(cs >> 5) * sizeof(uint32_t));
-            // a chunk cut inside a record leaves the words from ce on to the next chunk
-            rc = sbf::launch_query(f, k_seq, s.d_off, n_loc, k_out, s.stream, true, s.d_flag,
-                                   ce < hi ? (ce >> 5) : INT64_MAX);
+            // a chunk cut inside a record leaves the words from ce on to the next chunk.
+            // Checked whole: a whole chunk takes the call's uniformity flag (a
+            // uniform batch gives uniform whole chunks), a cut one none (CSR).
+            if (all_off)
+                rc = sbf::launch_query(f, k_seq, k_off, n_loc, k_out, s.stream, true, whole ? call_flag : nullptr,
+                                       ce < hi ? (ce >> 5) : INT64_MAX, false);
+            else
+                rc = sbf::launch_query(f, k_seq, k_off, n_loc, k_out, s.stream, true, s.d_flag,
+                                       ce < hi ? (ce >> 5) : INT64_MAX);
             if (rc != SBF_OK) break;
             if (stage_out) {
                 e = cudaMemcpyAsync(s.h_out, s.d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost,
@@ -344,7 +404,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
                 s.pend_words = words;
             }
         } else {
-            rc = sbf::launch_insert(f, k_seq, s.d_off, n_loc, s.stream, true);
+            rc = sbf::launch_insert(f, k_seq, k_off, n_loc, s.stream, true, !all_off);
             if (rc != SBF_OK) break;
         }
         cs = ce;
@@ -379,6 +439,8 @@ void sbf::destroy_stager(void *p) {
         cudaFreeHost(s.h_out);
         if (s.stream) cudaStreamDestroy(s.stream);
     }
+    cudaFree(st->d_all_off);
+    cudaFree(st->d_call_flag);
     delete st;
 }
 

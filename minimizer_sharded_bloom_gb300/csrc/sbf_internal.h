@@ -41,15 +41,19 @@ int set_error(int code, const char *fmt, ...);
 void destroy_stager(void *stager);
 // Launch the check + insert/query kernels; device_seq = false when seq is host
 // memory read in place (the kernel then loads tile bytes without TMA).
+// run_check = false: the caller has already checked these offsets on the
+// device (and, for a query, set flag_word from that check or passed nullptr).
 int launch_insert(sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n, void *stream,
-                  bool device_seq);
+                  bool device_seq, bool run_check = true);
 // flag_word: a device int the call may use to detect a uniform batch (the
 // no-alloc path passes one of its own); nullptr: allocated per call.
 // out_words_end: answer words at or past this index are left unwritten.
 int launch_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                  uint32_t *out_bits, void *stream, bool device_seq, int *flag_word = nullptr,
-                 int64_t out_words_end = INT64_MAX);
+                 int64_t out_words_end = INT64_MAX, bool run_check = true);
 // The device check of an offsets array (device-accessible) alone; a bad array
 // sets the sticky status, which every later launch of the filter honours.
-int launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream);
+// nonuniform (zeroed here first): set when record lengths differ.
+int launch_offsets_check(const sbf_filter *f, const int64_t *offsets, int64_t n, void *stream,
+                         int *nonuniform = nullptr);
 }  // namespace sbf
