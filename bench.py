@@ -130,7 +130,7 @@ ALU_PEAK_TOPS = 152 * 64 * 2.07e9 / 1e12
 MEASURED_TRAFFIC = {
     "out-of-cache": {"source_sha": "81fea15e301fb957", "insert": 14.4073, "query": 18.2213},
     "protein-like": {"source_sha": "5a8e9ca5e801e671", "insert": 37.0033, "query": 52.7077},
-    "triplet": {"source_sha": "5ec40e89a3fe204a", "insert": 33.3874, "query": 40.2951},
+    "triplet": {"source_sha": "5ec40e89a3fe204a", "insert": 33.3874, "query": None},
 }
 
 
@@ -377,16 +377,15 @@ def main():
                            alphabet=p["alphabet"])
     if p["alphabet"] == "dna" and not sbf.specialized:
         raise RuntimeError("the benchmark configuration must run its specialised kernel")
-    # which kernel runs each call: DNA and the protein point on the strip
-    # kernel; the triplet point inserts on the strip kernel and queries on the
-    # tiled alphabet kernel
+    # which kernel runs each call: DNA and the protein and triplet points on
+    # the strip kernel, other alphabet points on the tiled alphabet kernel
     pt = f"{p['k']},{p['m']},{p['s']},{p['H']}"
     an = "protein" if p["alphabet"] == "protein" else "triplet"
 
     def kname(kind):
         if p["alphabet"] == "dna":
             return f"strip_kernel<{pt},{kind}>"
-        if sbf.specialized and (p["alphabet"] == "protein" or kind == "insert"):
+        if sbf.specialized:
             return f"strip_kernel<{pt},{kind},{an}>"
         return f"alphabet_kernel<{an},{pt},{kind}>"
     stream = torch.cuda.current_stream()

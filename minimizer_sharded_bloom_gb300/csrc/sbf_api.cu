@@ -306,15 +306,6 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
         sbf::find_alphabet_strip(alphabet, k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
         threads_query = threads;
-        if (alphabet == SBF_ALPHABET_DNA_TRIPLET) {
-            // triplet queries of read batches mix the three frames inside every
-            // warp, so the strip kernel's frame passes cannot skip work there:
-            // the query keeps the tiled alphabet kernel
-            const void *unused = nullptr;
-            bool spec = false;
-            sbf::find_alphabet_kernels(alphabet, k, m, s, H, &unused, &qry, &spec);
-            threads_query = 256;
-        }
     } else if (alphabet != SBF_ALPHABET_DNA) {
         bool spec = false;
         sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec);
