@@ -24,6 +24,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "sbf_chunks.h"
 #include "sbf_internal.h"
 
 namespace {
@@ -147,20 +148,6 @@ int run_in_place(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, 
     return 1;
 }
 
-// Records searched back from a nominal chunk end for one that starts on an
-// answer-word boundary.
-constexpr int kEdgeSearch = 64;
-
-// First record r with offsets[r + 1] > g.
-int64_t record_at(const int64_t *off, int64_t n, int64_t g) {
-    int64_t lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int64_t mid = lo + (hi - lo) / 2;
-        if (off[mid + 1] > g) hi = mid; else lo = mid + 1;
-    }
-    return lo;
-}
-
 int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint32_t *out_bits,
              void *user_stream, bool query) {
     using sbf::set_error;
@@ -256,60 +243,19 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     cudaEventRecord(checked, reinterpret_cast<cudaStream_t>(user_stream));
 
     const int64_t kb = sbf::kmer_bytes(f);
-    const int sb = sbf::symbol_bytes(f->alphabet);
-    // Chunks start at 2^22 positions and double up to about an eighth of the
-    // batch (at most the filter's chunk setting): the first copy, which no
-    // kernel overlaps, stays short, and later ones are large.
-    const int64_t chunk_max = std::min<int64_t>(
-        f->host_chunk, std::max<int64_t>(((hi - lo) / 8 + 31) & ~int64_t(31), int64_t(1) << 22));
-    int64_t chunk = std::min<int64_t>(chunk_max, int64_t(1) << 22);
+    // the chunks and their clipped ends (sbf_chunks.h); a query's chunks also
+    // shrink towards the batch's end, an insert's do not (its kernels take
+    // longer than its copies, and small launches of its random updates cost
+    // throughput)
+    sbf::ChunkPlan plan(off, n, f->host_chunk, kb, sbf::symbol_bytes(f->alphabet), query);
+    const int64_t chunk_max = plan.chunk_max();
     int rc = SBF_OK;
-    // ... and for a query they shrink again towards the end (at most half of
-    // what is left), so that its last kernel, which no copy overlaps, is
-    // short too.  (An insert's kernels take longer than its copies, and
-    // small launches of its random updates cost throughput.)
-    int64_t cs = lo & ~int64_t(31);
-    for (int64_t c = 0; cs < hi && rc == SBF_OK; ++c) {
-        const int64_t data_lo = std::max<int64_t>(cs, lo);
-        const int64_t cur =
-            query ? std::min<int64_t>(chunk, std::max<int64_t>(((hi - cs) / 2 + 31) & ~int64_t(31),
-                                                               std::min<int64_t>(chunk, int64_t(1) << 22)))
-                  : chunk;
-        int64_t ce = std::min<int64_t>(cs + cur, hi);
-        int64_t data_hi = hi;
-        if (ce < hi) {
-            // End the chunk at a record start on an answer-word boundary when
-            // one is near: no record is cut (no k-mer overlap), and the chunk
-            // of a batch of equal-length reads still runs dense.  Else cut at
-            // ce and ship the k - 1 bytes after it.
-            int64_t P = -1;
-            int64_t r = record_at(off, n, ce);
-            for (int t = 0; t < kEdgeSearch && r > 0; ++t, --r) {
-                const int64_t p = off[r];
-                if (p <= data_lo) break;
-                if (p <= ce && (p & 31) == 0) {
-                    P = p;
-                    break;
-                }
-            }
-            if (P > 0) ce = data_hi = P;
-            else data_hi = std::min<int64_t>(ce + kb - 1, hi);
-        }
-        const int64_t r0 = record_at(off, n, data_lo);
-        const int64_t r1 = record_at(off, n, data_hi - 1) + 1;
-        if (r1 <= r0) {  // only with offsets the check rejects
-            cs = ce;
-            continue;
-        }
+    sbf::Chunk ch;
+    for (int64_t c = 0; rc == SBF_OK && plan.next(ch); ++c) {
+        if (ch.empty) continue;  // only with offsets the check rejects
+        const int64_t cs = ch.cs, ce = ch.ce, data_lo = ch.data_lo, data_hi = ch.data_hi;
+        const int64_t r0 = ch.r0, r1 = ch.r1, first = ch.first, last = ch.last;
         const int64_t n_loc = r1 - r0;
-        // The chunk's offsets are the caller's, absolute, with both ends
-        // clipped to [data_lo, data_hi]; a record cut at data_lo starts at its
-        // next symbol boundary (DNA triplets keep their codon frame).
-        auto clip = [&](int64_t v) { return std::min<int64_t>(std::max<int64_t>(v, data_lo), data_hi); };
-        const int64_t last = clip(off[r1]);
-        const int64_t next = n_loc >= 2 ? clip(off[r0 + 1]) : last;
-        int64_t first = off[r0] < data_lo ? data_lo + (sb - (data_lo - off[r0]) % sb) % sb : off[r0];
-        first = std::min<int64_t>(clip(first), next);
         const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel may write
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
         Slot &s = st.slot[c % 4];
@@ -342,7 +288,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)(data_hi - data_lo), cudaMemcpyHostToDevice, s.stream);
         const size_t off_bytes = sizeof(int64_t) * (size_t)(n_loc + 1);
         // both ends at record starts: the caller's slice as it is
-        const bool whole = first == off[r0] && last == off[r1];
+        const bool whole = ch.whole;
         const int64_t *k_off = s.d_off;
         if (all_off) {
             // from the device copy of the whole array (written before `checked`)
@@ -388,10 +334,10 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             // uniform batch gives uniform whole chunks), a cut one none (CSR).
             if (all_off)
                 rc = sbf::launch_query(f, k_seq, k_off, n_loc, k_out, s.stream, true, whole ? call_flag : nullptr,
-                                       ce < hi ? (ce >> 5) : INT64_MAX, false);
+                                       ch.final ? INT64_MAX : (ce >> 5), false);
             else
                 rc = sbf::launch_query(f, k_seq, k_off, n_loc, k_out, s.stream, true, s.d_flag,
-                                       ce < hi ? (ce >> 5) : INT64_MAX);
+                                       ch.final ? INT64_MAX : (ce >> 5));
             if (rc != SBF_OK) break;
             if (stage_out) {
                 e = cudaMemcpyAsync(s.h_out, s.d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost,
@@ -407,8 +353,6 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             rc = sbf::launch_insert(f, k_seq, k_off, n_loc, s.stream, true, !all_off);
             if (rc != SBF_OK) break;
         }
-        cs = ce;
-        chunk = std::min<int64_t>(2 * chunk, chunk_max);
     }
     for (Slot &s : st.slot) {
         if (!s.stream) continue;
