@@ -183,9 +183,10 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         int rc = SBF_OK;
         if (run_in_place(f, seq, off, n, out_bits, user_stream, query, &rc)) return rc;
     }
-    // Staged.  The offsets are checked once, on the device where it reads
-    // them in place (a bad array sets the sticky status: every chunk's kernel
-    // then returns at once), else on the host.
+    // Staged.  The offsets are checked once before any chunk's kernel runs:
+    // on a device copy of the whole array (queries, below), on the device
+    // reading them in place, or else on the host.  A bad array sets the
+    // sticky status, and every chunk's kernel then returns at once.
     const int64_t *off_dev = static_cast<const int64_t *>(device_alias(off, f->device));
     // answers go straight to the caller's buffer where the device can write it
     uint32_t *out_dev = nullptr;
