@@ -39,3 +39,27 @@ def test_fpr_positions_are_the_oracle_valid_kmers():
         want = sum(oracle.count_runs(seq[off[r]:off[r + 1]], np.array([0, off[r + 1] - off[r]]),
                                      k, k // 2, k - 2, 4, 1 << 20, 3, alphabet)[0] for r in sub)
         assert bench.fpr_count(qry, k, B) == want
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle arm, no GPU) prints one JSON
+    line with the metric, the impl tag, its cpu_baseline and an e2e object
+    with no host-device bytes."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.join(os.path.dirname(os.path.abspath(__file__)), "..")
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                          "--steps", "2", "--warmup", "1"], cwd=root, capture_output=True, text=True,
+                         timeout=300, check=True)
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "k-mers/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["metric"].startswith("k-mers/s insert & query")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "k-mers/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
