@@ -164,3 +164,26 @@ def test_small_batch_is_one_chunk(driver):
     chunk_max, chunks = plan(driver, off, 1 << 26, 31, 1, True)
     assert len(chunks) == 1 and chunks[0]["whole"] == 1 and chunks[0]["final"] == 1
     check_plan(off, chunk_max, chunks, 1 << 26, 31, 1, True)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_malformed_offsets_still_plan_inside_the_batch(driver, seed):
+    """Offsets that decrease somewhere (the device check rejects them, but the
+    copies are issued before its verdict) still give a finite plan whose byte
+    ranges, record ranges and clipped ends all stay inside the batch."""
+    rng = np.random.default_rng(700 + seed)
+    n = 500
+    off = synth.csr(rng.integers(1, 400, size=n))
+    bad = rng.choice(np.arange(1, n), size=20, replace=False)
+    off[bad] = rng.integers(off[0], off[-1], size=bad.size)  # out of order
+    lo, hi = int(off[0]), int(off[-1])
+    chunk_max, chunks = plan(driver, off, 4096, 31, 1, True)
+    assert chunks and chunks[-1]["ce"] == hi
+    assert len(chunks) <= (hi - (lo & ~31)) // 32 + 1
+    for c in chunks:
+        assert lo & ~31 <= c["cs"] < c["ce"] <= hi
+        assert lo <= c["data_lo"] <= c["data_hi"] <= hi
+        assert c["data_hi"] - c["cs"] <= chunk_max + 31
+        if not c["empty"]:
+            assert 0 <= c["r0"] < c["r1"] <= n
+            assert c["data_lo"] <= c["first"] <= c["data_hi"] and c["data_lo"] <= c["last"] <= c["data_hi"]
