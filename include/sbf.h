@@ -177,7 +177,11 @@ int sbf_query_host(const sbf_filter *f, const char *seq, const int64_t *offsets,
  * that device current; make that first call before any stream capture.
  * All calls share the array: calls whose work overlaps on the GPU (e.g. on two
  * streams) race.  Work is ordered on `stream`; returns when out_bits is
- * complete. */
+ * complete.  Like sbf_query_host it ends by reading and clearing the filter's
+ * sticky status: if that status was set (this batch's offsets, or an earlier
+ * device call's not yet reported with sbf_get_status), the kernel skipped its
+ * work, the call returns SBF_ERR_BAD_OFFSETS (or SBF_ERR_CUDA after a device
+ * wait gave up), and the words copied to out_bits are not answers. */
 int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, const int64_t *offsets, int64_t n,
                            uint32_t *out_bits, void *stream);
 

@@ -10,10 +10,15 @@
 //
 // The array exists once per device that loads this library and stays
 // allocated until the process exits.  Every call shares it and it keeps the
-// previous call's contents; nothing in it needs clearing, because the query
-// kernel reads only the bytes and offsets copied in by the same call and writes
-// every answer word that is copied back.  Calls whose work overlaps on the GPU
-// (for example on two streams) race on the array.
+// previous call's contents.  The query kernel reads only the bytes and offsets
+// copied in by the same call, and when it runs it writes every answer word
+// that is copied back.  It does not run when the filter's sticky status is
+// already set (malformed offsets of an earlier call not yet reported, or a
+// bounded device wait that gave up): the staged answer words then hold an
+// earlier call's contents.  So the call ends like sbf_query_host, by reading
+// and clearing the status, and returns its error instead of those words'
+// meaning.  Calls whose work overlaps on the GPU (for example on two streams)
+// race on the array.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -105,5 +110,8 @@ extern "C" int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, cons
     e = cudaMemcpyAsync(out_bits + (cs >> 5), d_out, sizeof(uint32_t) * (size_t)words, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return set_error(SBF_ERR_CUDA, "sbf_query_host_noalloc: %s", cudaGetErrorString(e));
-    return SBF_OK;
+    // a set status means the kernel skipped its work and the copied words are
+    // stale: report it (and clear it) as sbf_query_host does; this reads one
+    // int with cudaMemcpy and allocates nothing
+    return sbf_get_status(const_cast<sbf_filter *>(f), stream);
 }

@@ -76,3 +76,46 @@ def test_noalloc_query_rejects_batches_beyond_its_limit():
         assert not out.any()
     finally:
         N.sbf_destroy(f)
+
+
+def test_noalloc_query_reports_a_pending_bad_offsets_status():
+    """A device-facing query with decreasing offsets sets the filter's sticky
+    status and nobody reads it.  The next no-alloc call must not hand back the
+    staging array's stale words as answers: the query kernel skips its work
+    while the status is set, so the call reports SBF_ERR_BAD_OFFSETS (and
+    clears the status); the call after it answers normally."""
+    torch = need_gpu()
+    from minimizer_sharded_bloom_gb300 import _native as N
+    L = N.load()
+    rng = np.random.default_rng(777)
+    ins = synth.random_records(rng, 20, 100, 3000, n_prob=0.002)
+    f = N.sbf_create(1 << 18, MAIN["k"], MAIN["m"], MAIN["s"], MAIN["H"], 5)
+    try:
+        N.sbf_insert_host(f, ins.seq.ctypes.data, ins.offsets.ctypes.data, ins.n_records)
+        # a good no-alloc call first, so the staging array holds real answers
+        first = np.zeros(_words(ins.offsets), dtype=np.uint32)
+        assert L.sbf_query_host_noalloc(f, ins.seq.ctypes.data, ins.offsets.ctypes.data, ins.n_records,
+                                        first.ctypes.data, None) == N.SBF_OK, N.last_error()
+        assert first.any()
+        # device-facing query with decreasing offsets; its status is left unread
+        dseq = torch.from_numpy(ins.seq.copy()).cuda()
+        bad = torch.tensor([0, 500, 200, 900], dtype=torch.int64, device="cuda")
+        dout = torch.zeros(64, dtype=torch.int32, device="cuda")
+        N.sbf_query(f, dseq.data_ptr(), bad.data_ptr(), 3, dout.data_ptr())
+        torch.cuda.synchronize()
+        # the same batch again through the no-alloc call: the error, not answers
+        stale = np.zeros(_words(ins.offsets), dtype=np.uint32)
+        rc = L.sbf_query_host_noalloc(f, ins.seq.ctypes.data, ins.offsets.ctypes.data, ins.n_records,
+                                      stale.ctypes.data, None)
+        assert rc == N.SBF_ERR_BAD_OFFSETS, (rc, N.last_error())
+        # the status was cleared: the next call matches the allocating query
+        got = np.zeros(_words(ins.offsets), dtype=np.uint32)
+        want = np.zeros(_words(ins.offsets), dtype=np.uint32)
+        assert L.sbf_query_host_noalloc(f, ins.seq.ctypes.data, ins.offsets.ctypes.data, ins.n_records,
+                                        got.ctypes.data, None) == N.SBF_OK, N.last_error()
+        N.sbf_query_host(f, ins.seq.ctypes.data, ins.offsets.ctypes.data, ins.n_records, want.ctypes.data)
+        lo, hi = int(ins.offsets[0]) >> 5, (int(ins.offsets[-1]) + 31) >> 5
+        assert np.array_equal(got[lo:hi], want[lo:hi])
+        assert np.array_equal(got[lo:hi], first[lo:hi])
+    finally:
+        N.sbf_destroy(f)
