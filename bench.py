@@ -118,11 +118,14 @@ def alu_ops(p):
     s-mer (k-s+1 of them); a codon decodes from three bases (+2)."""
     front = 39 + (2 if p["alphabet"] == "dna_triplet" else 0)
     return {"insert": front + 10, "query": front + 4 * (p["k"] - p["s"] + 1) + 10}
-# ALU-pipe peak: 152 SMs x 4 sub-partitions x 16 lanes x 2.07 GHz (maximum SM
-# clock).  ncu reports the ALU pipe at 16 lanes per sub-partition: with the
-# pipe ~75 % busy the issue rate is ~53 %, i.e. one ALU warp-instruction per
-# two cycles at most.
-ALU_PEAK_TOPS = 152 * 64 * 2.07e9 / 1e12
+# The ALU-pipe ceiling is measured in each run (probe kernels of
+# libsbf_probes.so: a LOP3 / funnel-shift / compare / select / min mix on
+# every SM, SM count from the device properties); see measure_ceilings().
+
+# The form of the shard updates and loads in the current kernel source, whose
+# probe rate is the pattern ceiling the insert and query are reported against.
+INSERT_FLUSH_FORM = "red4"      # one thread issues a run's four 64-bit OR reductions
+QUERY_SHARD_FORM = "cp_async"   # two 16-byte cp.async.cg copies per run head's shard
 
 # ncu DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per k-mer of
 # the full-size launches of each workload (summaries under profiles/), valid
@@ -241,6 +244,22 @@ def runs_estimate(wl, k=K, m=M, B=1):
     return kmer_count(wl, k, B) * 2.0 / (w + 1) + wl.n_records
 
 
+def exact_runs(workload: str, role: str, wl, p, bits, k=K, m=M, B=1):
+    """(runs, source): the oracle's exact run count of this input (stored in
+    oracle/run_counts.json by oracle/run_counts.py, matched by the input's
+    fingerprint and parameters), else the 2/(w+1) estimate."""
+    try:
+        with open(os.path.join(ROOT, "oracle", "run_counts.json")) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        rec = None
+    if rec and role in rec and rec.get("filter_bits") == bits and all(rec.get(x) == p[x] for x in ("k", "m", "s", "H")) \
+            and rec.get("alphabet") == p["alphabet"] and rec.get("seed") == SEED \
+            and rec[role]["fingerprint"] == synth.fingerprint(wl.seq, wl.offsets):
+        return float(rec[role]["runs"]), "exact (oracle run count of this input)"
+    return runs_estimate(wl, k, m, B), "estimate 2/(w+1) per k-mer + 1 per record (no stored count matches)"
+
+
 def fpr_count(qry, k=K, B=1) -> int:
     rnd = qry.meta.get("is_random")
     if rnd is None:
@@ -267,7 +286,8 @@ def fpr_of(words: np.ndarray, qry, k=K, B=1) -> float | None:
     return hits / total if total else None
 
 
-def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int = 300_000, p=MAIN):
+def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int = 300_000, p=MAIN,
+                 single_thread: bool = False):
     """The CPU oracle, as it stands, on a bounded prefix sample of the same
     workload, all host cores."""
     import oracle
@@ -290,11 +310,31 @@ def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int
     t2 = time.perf_counter()
     nk_i, nk_q = kmer_count(s_ins, k, B), kmer_count(s_q, k, B)
     nk = nk_i + nk_q
-    return {"value": nk / (t2 - t0), "unit": "k-mers/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {s_ins.n_bases:,} bytes ({r} records) inserted, first {rq:,} reads "
-                      f"queried; {nk:,} k-mers in {t2 - t0:.1f} s",
-            "insert_kmers_per_s": nk_i / (t1 - t0),
-            "query_kmers_per_s": nk_q / (t2 - t1)}
+    res = {"value": nk / (t2 - t0), "unit": "k-mers/s", "cores": cores, "kind": "oracle",
+           "sample": f"first {s_ins.n_bases:,} bytes ({r} records) inserted, first {rq:,} reads "
+                     f"queried; {nk:,} k-mers in {t2 - t0:.1f} s",
+           "insert_kmers_per_s": nk_i / (t1 - t0),
+           "query_kmers_per_s": nk_q / (t2 - t1)}
+    if single_thread:
+        # the same loops on one thread, on a tenth of the sample
+        e1 = int(ins.offsets[0]) + budget_bases // 10
+        o1 = np.minimum(ins.offsets, e1)
+        r1 = max(1, min(int(np.searchsorted(o1, e1, side="left")), ins.n_records))
+        w_ins = synth.Workload(ins.seq[:o1[r1]], o1[:r1 + 1])
+        rq1 = max(1, min(reads // 10, qry.n_records))
+        w_q = synth.Workload(qry.seq[:qry.offsets[rq1]], qry.offsets[:rq1 + 1])
+        F1 = oracle.new_filter(bits)
+        u0 = time.perf_counter()
+        oracle.insert(F1, w_ins.seq, w_ins.offsets, k, m, s, h, SEED, nthreads=1, alphabet=p["alphabet"])
+        u1 = time.perf_counter()
+        oracle.query(F1, w_q.seq, w_q.offsets, k, m, s, h, SEED, nthreads=1, alphabet=p["alphabet"])
+        u2 = time.perf_counter()
+        n1, n2 = kmer_count(w_ins, k, B), kmer_count(w_q, k, B)
+        res["single_thread"] = {"kmers_per_s": (n1 + n2) / (u2 - u0), "cores": 1,
+                                "insert_kmers_per_s": n1 / (u1 - u0), "query_kmers_per_s": n2 / (u2 - u1),
+                                "sample": f"first {w_ins.n_bases:,} bytes inserted, first {rq1:,} reads queried"}
+        res["single_thread_kmers_per_s"] = res["single_thread"]["kmers_per_s"]
+    return res
 
 
 def run_reference(args, workload):
@@ -329,7 +369,7 @@ def run_reference(args, workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="out-of-cache", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -392,16 +432,19 @@ def main():
     sh = int(stream.cuda_stream)
     n_ins, n_q = ins.n_records, qry.n_records
 
+    def clear():
+        # untimed: every insert starts from an empty filter (the 2^36-bit
+        # memset also evicts the inputs and the filter from L2)
+        N.sbf_clear(sbf.handle, sh)
+
     def step():
         N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
         N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), n_q, out.data_ptr(), sh)
 
-    # the random-RMW ceiling (an 8 GiB probe) for filters larger than L2,
-    # except at the profiling sizes
-    rmw_gib = max(1, spec["bits"] >> 33)  # the probe spans the filter's size
-    rmw_ceiling = (random_rmw_ceiling(torch, gib=rmw_gib)
-                   if spec["bits"] > 8 * (129 << 20) and not args.workload.endswith("-small") else None)
+    # hardware ceilings of this GPU, measured before the timed region
+    ceil = measure_ceilings(torch, spec["bits"], small=args.workload.endswith("-small") or spec["bits"] < (1 << 30))
     for _ in range(max(args.warmup, 0)):
+        clear()
         step()
     torch.cuda.synchronize()
     if sbf.status() != 0:
@@ -414,6 +457,7 @@ def main():
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
+        clear()
         ev[i][0].record(stream)
         N.sbf_insert(sbf.handle, dseq.data_ptr(), doff.data_ptr(), n_ins, sh)
         ev[i][1].record(stream)
@@ -426,8 +470,11 @@ def main():
     clocks = sampler.stop() if sampler else None
     t_ins = [ev[i][0].elapsed_time(ev[i][1]) / 1e3 for i in range(args.steps)]
     t_q = [ev[i][1].elapsed_time(ev[i][2]) / 1e3 for i in range(args.steps)]
-    total = sum(t_ins) + sum(t_q)
-    total, s_ins, s_q = max_over_ranks(pg, [total, sum(t_ins), sum(t_q)])
+    # per call: the median of the event-timed calls (the slowest rank's);
+    # the means are kept for the roofline's average launch duration
+    med_ins, med_q, mean_ins, mean_q = max_over_ranks(
+        pg, [statistics.median(t_ins), statistics.median(t_q), statistics.mean(t_ins), statistics.mean(t_q)])
+    step_s = med_ins + med_q
     if sbf.status() != 0:
         raise RuntimeError("device status error in the timed region")
 
@@ -438,6 +485,7 @@ def main():
     # sbf_query_dense, timed apart from the step, its answers checked equal
     dense = None
     lens = np.diff(qry.offsets)
+    alu_peak = ceil["alu"]["ops_per_s"] / 1e12
     if p["alphabet"] == "dna" and lens.size and (lens == lens[0]).all() and qry.offsets[0] == 0:
         rl = int(lens[0])
         dout = torch.zeros_like(out)
@@ -448,19 +496,18 @@ def main():
         same = bool(torch.equal(dout[: (qry.n_bases + 31) // 32], out[: (qry.n_bases + 31) // 32]))
         dense = {"call": "sbf_query_dense", "record_len": rl, "kmers_per_s": nk_q / t_dense,
                  "ms": 1e3 * t_dense, "answers_equal_csr": same,
-                 "alu_frac": alu_ops(p)["query"] * nk_q / t_dense / 1e12 / ALU_PEAK_TOPS,
+                 "alu_frac": alu_ops(p)["query"] * nk_q / t_dense / 1e12 / alu_peak,
                  "note": "one strip per read (skips the k-1 tail positions of each read); "
-                         "not part of `value`, which uses the CSR query"}
+                         "not part of `value`, which uses the CSR query (it runs this batch dense too)"}
         del dout
-    value = throughput(world, args.steps, nk_ins + nk_q, total)
+    value = throughput(world, 1, nk_ins + nk_q, step_s)
 
     # rooflines: insert against HBM (one 32-byte sector read and written per
     # run), query against the ALU pipe; "roofline" is the dominant (longer) one.
     peaks, peak_src = measured_peaks()
-    avg_ins, avg_q = s_ins / args.steps, s_q / args.steps
     sha = kernel_source_sha(p)
-    runs_i = runs_estimate(ins, p["k"], p["m"], B)
-    runs_q = runs_estimate(qry, p["k"], p["m"], B)
+    runs_i, runs_i_src = exact_runs(args.workload, "insert", ins, p, spec["bits"], p["k"], p["m"], B)
+    runs_q, runs_q_src = exact_runs(args.workload, "query", qry, p, spec["bits"], p["k"], p["m"], B)
     ops = alu_ops(p)
     bytes_ins = ins.n_bases + 8 * (n_ins + 1) + 64 * runs_i
     bytes_q = qry.n_bases + 8 * (n_q + 1) + 32 * runs_q + 4 * ((qry.n_bases + 31) // 32)
@@ -471,30 +518,43 @@ def main():
             return rec[name] * nk
         return None
 
-    ins_ach = bytes_ins / avg_ins / 1e9
+    ins_ach = bytes_ins / mean_ins / 1e9
     roof_ins = {"bound": "hbm", "kernel": kname("insert"),
                 "achieved": ins_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ins_ach / peaks["hbm_gbs"], "traffic": traffic_of("insert", nk_ins),
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
                 "algorithmic_bytes_per_kmer": bytes_ins / nk_ins,
-                "runs_per_launch": runs_i, "avg_launch_ms": 1e3 * avg_ins}
-    if rmw_ceiling:
+                "runs_per_launch": runs_i, "runs_source": runs_i_src,
+                "avg_launch_ms": 1e3 * mean_ins, "median_launch_ms": 1e3 * med_ins}
+    rmw = ceil["rmw"].get(INSERT_FLUSH_FORM)
+    if rmw:
         roof_ins["pattern_peak"] = {
-            "what": "random 32-byte row read-modify-write (4 x 64-bit atomic add per row, "
-                    f"torch index_add_) over a {rmw_gib} GiB tensor (the filter's size), measured in this run",
-            "rows_per_s": rmw_ceiling, "runs_per_s": runs_i / avg_ins,
-            "frac": runs_i / avg_ins / rmw_ceiling}
-    q_ach = ops["query"] * nk_q / avg_q / 1e12
+            "what": f"random 32-byte row read-modify-writes over a {rmw['buffer_gib']:.0f} GiB buffer, "
+                    f"hand-written probe in the insert's flush form ({INSERT_FLUSH_FORM}), measured in this run",
+            "form": INSERT_FLUSH_FORM, "rows_per_s": rmw["rows_per_s"], "runs_per_s": runs_i / mean_ins,
+            "frac": runs_i / mean_ins / rmw["rows_per_s"],
+            "all_forms_rows_per_s": {k: v["rows_per_s"] for k, v in ceil["rmw"].items()}}
+    q_ach = ops["query"] * nk_q / mean_q / 1e12
     roof_q = {"bound": "alu", "kernel": kname("query"),
-              "achieved": q_ach, "peak": ALU_PEAK_TOPS, "unit": "Tops/s (ALU pipe)",
-              "frac": q_ach / ALU_PEAK_TOPS, "traffic": traffic_of("query", nk_q),
-              "peak_source": "152 SMs x 64 ALU lanes x 2.07 GHz (recipe SM count and clock)",
-              "ops_per_kmer": ops["query"], "avg_launch_ms": 1e3 * avg_q,
-              "algorithmic_bytes_per_kmer": bytes_q / nk_q,
-              "hbm_frac": bytes_q / avg_q / 1e9 / peaks["hbm_gbs"]}
-    ins_alu = ops["insert"] * nk_ins / avg_ins / 1e12
-    roof_ins["alu_frac"] = ins_alu / ALU_PEAK_TOPS
-    roofline, roofline_other = (roof_ins, roof_q) if avg_ins >= avg_q else (roof_q, roof_ins)
+              "achieved": q_ach, "peak": alu_peak, "unit": "Tops/s (ALU pipe)",
+              "frac": q_ach / alu_peak, "traffic": traffic_of("query", nk_q),
+              "peak_source": f"measured in this run: probe of a LOP3/SHF/ISETP/SEL/IMNMX mix on all "
+                             f"{ceil['sms']} SMs ({ceil['alu']['ops_per_sm_clock_at_2070MHz']:.1f} ops/SM/clock "
+                             f"at 2.07 GHz)",
+              "ops_per_kmer": ops["query"], "avg_launch_ms": 1e3 * mean_q, "median_launch_ms": 1e3 * med_q,
+              "algorithmic_bytes_per_kmer": bytes_q / nk_q, "runs_per_launch": runs_q, "runs_source": runs_q_src,
+              "hbm_frac": bytes_q / mean_q / 1e9 / peaks["hbm_gbs"]}
+    rd = ceil["read"].get(QUERY_SHARD_FORM)
+    if rd:
+        roof_q["pattern_peak"] = {
+            "what": f"random 32-byte row reads over a {rd['buffer_gib']:.0f} GiB buffer, hand-written probe in "
+                    f"the query's shard-load form ({QUERY_SHARD_FORM}), measured in this run",
+            "form": QUERY_SHARD_FORM, "rows_per_s": rd["rows_per_s"], "runs_per_s": runs_q / mean_q,
+            "frac": runs_q / mean_q / rd["rows_per_s"],
+            "all_forms_rows_per_s": {k: v["rows_per_s"] for k, v in ceil["read"].items()}}
+    ins_alu = ops["insert"] * nk_ins / mean_ins / 1e12
+    roof_ins["alu_frac"] = ins_alu / alu_peak
+    roofline, roofline_other = (roof_ins, roof_q) if mean_ins >= mean_q else (roof_q, roof_ins)
 
     e2e = None
     if not args.no_e2e:
@@ -502,17 +562,17 @@ def main():
             N.sbf_set_host_mode(sbf.handle, args.host_mode)
         if args.host_chunk is not None:
             N.sbf_set_host_chunk(sbf.handle, args.host_chunk)
-        e2e = run_e2e(torch, N, sbf, ins, qry, nk_ins + nk_q, pg, world, min(args.steps, 3))
+        e2e = run_e2e(torch, N, sbf, ins, qry, nk_ins + nk_q, pg, world, max(args.steps, 10))
 
     cb = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = cpu_baseline(ins, qry, spec["bits"], p=p)
+        cb = cpu_baseline(ins, qry, spec["bits"], p=p, single_thread=True)
 
     if rank == 0:
         line = {
             "metric": metric_of(p), "value": value, "unit": "k-mers/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "ms_per_step": 1e3 * step_s, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64 (integer)",
             "data": "synthetic",
             "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
@@ -523,15 +583,23 @@ def main():
                               "protein-like": "inputs larger than L2 (sequences 0.5 GB each, filter 1 GiB)",
                               "triplet": "inputs larger than L2 (sequences 1 GB each, filter 1 GiB)"}
                              .get(args.workload, "see workload"),
-                       "filter_between_steps": "not cleared (insert is idempotent; same work)",
+                       "filter_between_steps": "zeroed before every insert (sbf_clear, untimed, outside "
+                                               "the events; it also flushes L2)",
+                       "timing": "CUDA events around each call on the launching stream; value and "
+                                 "ms_per_step from the median insert + median query",
                        "replicas": world},
-            "insert_kmers_per_s": throughput(world, args.steps, nk_ins, s_ins),
-            "query_kmers_per_s": throughput(world, args.steps, nk_q, s_q),
+            "insert_kmers_per_s": throughput(world, 1, nk_ins, med_ins),
+            "query_kmers_per_s": throughput(world, 1, nk_q, med_q),
+            "insert_ms": {"median": 1e3 * med_ins, "mean": 1e3 * mean_ins, "all": [1e3 * t for t in t_ins]},
+            "query_ms": {"median": 1e3 * med_q, "mean": 1e3 * mean_q, "all": [1e3 * t for t in t_q]},
+            "value_from_means": throughput(world, 1, nk_ins + nk_q, mean_ins + mean_q),
             "fpr": fpr, "fpr_definition": "answer-positive fraction of the valid k-mers of the uniform reads",
             "query_dense": dense,
             "roofline": roofline, "roofline_other_kernel": roofline_other,
+            "ceilings": ceil,
             "gpu_launches": 4 * args.steps,
-            "gpu_launches_note": "per step: offsets check + insert kernel, offsets check + query kernel",
+            "gpu_launches_note": "per step: offsets check + insert kernel, offsets check + query kernel "
+                                 "(the untimed filter clear is a memset)",
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cb,
             "wall_s_timed": t_wall,
         }
@@ -541,28 +609,24 @@ def main():
         pg.destroy_process_group()
 
 
-def random_rmw_ceiling(torch, gib: int = 8, rows_touched: int = 25_000_000) -> float:
-    """Rows per second of random 32-byte read-modify-writes over a gib-GiB
-    tensor (torch index_add_: four 64-bit atomic adds per row) -- the memory
-    system's ceiling for the insert's per-run shard update."""
-    n_rows = (gib << 30) // 32
-    F = torch.zeros(n_rows, 4, dtype=torch.int64, device="cuda")
-    g = torch.Generator(device="cuda").manual_seed(1)
-    idx = torch.randint(0, n_rows, (rows_touched,), device="cuda", generator=g)
-    src = torch.ones(rows_touched, 4, dtype=torch.int64, device="cuda")
-    for _ in range(2):
-        F.index_add_(0, idx, src)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(3):
-        F.index_add_(0, idx, src)
-    e1.record()
-    torch.cuda.synchronize()
-    rate = 3 * rows_touched / (e0.elapsed_time(e1) / 1e3)
-    del F, idx, src
+def measure_ceilings(torch, filter_bits: int, small: bool = False) -> dict:
+    """The ceilings of this GPU, from the hand-written probe kernels
+    (libsbf_probes.so): the ALU instruction rate of the mix the filter
+    kernels issue, on all SMs; scattered 32-byte row read-modify-writes and
+    reads over a buffer of the filter's size (at least 1 GiB, so not
+    L2-resident), in every form the kernels may use; ~120 M rows each (the
+    out-of-cache insert's run count)."""
+    from minimizer_sharded_bloom_gb300 import probes
+    res = {"sms": probes.sm_count(), "alu": probes.alu_rate(torch, "mix")}
+    res["alu_imad"] = probes.alu_rate(torch, "imad")
+    gib = max(1, filter_bits >> 33)
+    n = 30_000_000 if small else 118_000_000
+    buf = torch.zeros((gib << 30) // 8, dtype=torch.int64, device="cuda")
+    res["rmw"] = {m: probes.rmw_rate(torch, m, n_updates=n, buf=buf) for m in ("red4", "red_queue")}
+    res["read"] = {m: probes.read_rate(torch, m, n_reads=n, buf=buf) for m in ("ld_nc", "cp_async", "bulk32")}
+    del buf
     torch.cuda.empty_cache()
-    return rate
+    return res
 
 
 def _timed(torch, fn, warmup=2, reps=3):
@@ -670,35 +734,65 @@ def run_suite(args):
 def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
     """Same metric through the host-facing C-ABI calls: pinned host inputs,
     host-to-device copies and the answer's device-to-host copy inside the
-    timed region (each call synchronizes)."""
+    timed region (each call synchronizes).  The filter is zeroed before each
+    step, outside the timed region.  Each call is timed on the host clock;
+    the value uses the median step, and the per-call medians and maxima plus
+    the host link's copy rate (1 GiB from the same kind of pinned buffer,
+    CUDA events) are reported beside it."""
     h_seq = torch.from_numpy(ins.seq).pin_memory()
     h_off = torch.from_numpy(ins.offsets).pin_memory()
     h_q = torch.from_numpy(qry.seq).pin_memory()
     h_qo = torch.from_numpy(qry.offsets).pin_memory()
     h_out = torch.zeros((qry.n_bases + 31) // 32 + 1, dtype=torch.int32).pin_memory()
+    sh = int(torch.cuda.current_stream().cuda_stream)
 
     def one():
-        N.sbf_insert_host(sbf.handle, h_seq.data_ptr(), h_off.data_ptr(), ins.n_records, 0)
-        N.sbf_query_host(sbf.handle, h_q.data_ptr(), h_qo.data_ptr(), qry.n_records,
-                         h_out.data_ptr(), 0)
+        N.sbf_clear(sbf.handle, sh)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        N.sbf_insert_host(sbf.handle, h_seq.data_ptr(), h_off.data_ptr(), ins.n_records, sh)
+        t1 = time.perf_counter()
+        N.sbf_query_host(sbf.handle, h_q.data_ptr(), h_qo.data_ptr(), qry.n_records, h_out.data_ptr(), sh)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
 
-    for _ in range(2):  # the first calls size the staging buffers
+    for _ in range(3):  # the first calls size the staging buffers
         one()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    t0 = time.perf_counter()
+    ti, tq = [], []
     for _ in range(steps):
-        one()
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    dt = max_over_ranks(pg, [dt])[0]
+        a, b = one()
+        ti.append(a)
+        tq.append(b)
+    tstep = [a + b for a, b in zip(ti, tq)]
+    med, mean, worst = max_over_ranks(pg, [statistics.median(tstep), statistics.mean(tstep), max(tstep)])
+    # the host link, measured now: 1 GiB from pinned memory to the device
+    hb = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    db = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    link = []
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        db.copy_(hb, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        link.append((1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del hb, db
     h2d = ins.seq.nbytes + ins.offsets.nbytes + qry.seq.nbytes + qry.offsets.nbytes
     d2h = 4 * ((qry.n_bases + 31) // 32)
-    return {"value": throughput(world, steps, nk_total, dt), "unit": "k-mers/s",
+    ms = [1e3 * x for x in (statistics.median(ti), max(ti), statistics.median(tq), max(tq))]
+    return {"value": throughput(world, 1, nk_total, med), "unit": "k-mers/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "path": "sbf_insert_host + sbf_query_host, pinned host buffers, host wall clock"}
+            "steps": steps, "ms_per_step": 1e3 * med, "ms_per_step_mean": 1e3 * mean,
+            "ms_per_step_max": 1e3 * worst, "value_from_mean": throughput(world, 1, nk_total, mean),
+            "insert_host_ms": {"median": ms[0], "max": ms[1]},
+            "query_host_ms": {"median": ms[2], "max": ms[3]},
+            "link_h2d_gbs": statistics.median(link),
+            "link_bound_ms_per_step": 1e3 * h2d / (statistics.median(link) * 1e9),
+            "path": "sbf_insert_host + sbf_query_host, pinned host buffers, host clock per call; "
+                    "filter zeroed before each step (untimed)"}
 
 
 if __name__ == "__main__":

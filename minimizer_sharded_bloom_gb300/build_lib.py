@@ -1,8 +1,9 @@
 """Build libsbf.so in-tree with nvcc for GB300 (sm_103a).
 
 Every .cu unit under csrc/ compiles in parallel to an object under _build/,
-then nvcc links the shared library _build/libsbf.so.  Objects are rebuilt when
-their source or any header is newer.
+then nvcc links the shared library _build/libsbf.so.  The benchmark's ceiling
+probes (probes/*.cu) link into _build/libsbf_probes.so the same way.  Objects
+are rebuilt when their source or any header is newer.
 """
 from __future__ import annotations
 
@@ -16,6 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsbf.so")
+PROBES = os.path.join(HERE, "probes")
+PROBE_LIB = os.path.join(OUT, "libsbf_probes.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -46,9 +49,13 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+def probe_sources():
+    return sorted(glob.glob(os.path.join(PROBES, "*.cu")))
+
+
 def _headers_mtime() -> float:
     hs = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-    hs.append(os.path.join(INCLUDE, "sbf.h"))
+    hs += glob.glob(os.path.join(INCLUDE, "*.h"))
     return max(os.path.getmtime(h) for h in hs)
 
 
@@ -69,24 +76,31 @@ def _compile(src: str, hdr_time: float, verbose: bool) -> str:
     return obj
 
 
+def _link(lib: str, objs, extra) -> None:
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(o) for o in objs):
+        return
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs] + extra
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, lib)
+
+
 def build(jobs: int | None = None, verbose: bool = False) -> str:
-    """Compile and link libsbf.so; returns its path."""
+    """Compile and link libsbf.so and libsbf_probes.so; returns libsbf's path."""
     os.makedirs(OUT, exist_ok=True)
     hdr = _headers_mtime()
     srcs = sources()
     # the heavy specialisation units first
     srcs.sort(key=lambda s: ("sbf_inst" not in s, s))
-    jobs = jobs or max(1, min(len(srcs), os.cpu_count() or 1))
+    psrcs = probe_sources()
+    jobs = jobs or max(1, min(len(srcs) + len(psrcs), os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, hdr, verbose), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs] + (["-lz"] if ZLIB else [])
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
+        objs = list(ex.map(lambda s: _compile(s, hdr, verbose), srcs + psrcs))
+    _link(LIB, objs[:len(srcs)], ["-lz"] if ZLIB else [])
+    if psrcs:
+        _link(PROBE_LIB, objs[len(srcs):], [])
     return LIB
 
 

@@ -38,6 +38,18 @@ ACGT = np.frombuffer(b"ACGT", dtype=np.uint8)
 AMINO20 = np.frombuffer(b"ACDEFGHIKLMNPQRSTVWY", dtype=np.uint8)
 
 
+def fingerprint(seq: np.ndarray, offsets: np.ndarray) -> str:
+    """A short identity of a generated input: sha256 of the offsets, every
+    4,097th byte of the sequence and its length.  Lets a stored per-input
+    count be matched to the input it was computed on."""
+    import hashlib
+    h = hashlib.sha256()
+    h.update(np.ascontiguousarray(offsets, dtype=np.int64).tobytes())
+    h.update(np.ascontiguousarray(seq[::4097]).tobytes())
+    h.update(str(seq.size).encode())
+    return h.hexdigest()[:32]
+
+
 def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 

@@ -82,3 +82,20 @@ def test_create_without_gpu_fails_cleanly(lib):
     L = _native.load()
     assert not L.sbf_create(1 << 20, 31, 16, 28, 4, 0)
     assert _native.last_error()
+
+
+def test_probe_library_exports_every_declared_symbol(lib):
+    """The benchmark's ceiling probes (include/sbf_probes.h) are a library of
+    their own; every declared entry point is exported, the binding loads them
+    all, and invalid arguments are refused before any launch."""
+    from minimizer_sharded_bloom_gb300 import build_lib, probes
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "sbf_probes.h")).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(sbf_probe_[a-z_]+)\s*\(", text)))
+    assert names == ["sbf_probe_alu", "sbf_probe_read", "sbf_probe_rmw", "sbf_probe_sm_count"]
+    P = ctypes.CDLL(build_lib.PROBE_LIB)
+    for name in names:
+        assert hasattr(P, name), name
+    L = probes.load()
+    assert L.sbf_probe_rmw(0, None, 3, 1, 1, 1, 32, None) == -1       # no buffer, rows not a power of two
+    assert L.sbf_probe_read(9, None, 4, 1, 1, 1, 32, None, None) == -1  # unknown mode
+    assert L.sbf_probe_alu(7, 1, 1, 32, None, None, None) == -1         # unknown kind
