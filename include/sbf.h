@@ -283,6 +283,17 @@ int sbf_get_params(const sbf_filter *f, int *k, int *m, int *s, int *H, uint64_t
  * (k, m, s, H), 0 if they run the runtime-parameter kernel (same results). */
 int sbf_is_specialized(const sbf_filter *f);
 
+/* Failure-detection test hook (the paper has no counterpart).  Launches the
+ * filter's insert kernel once so that one thread waits on an mbarrier that
+ * nothing completes (no copy attached), giving up after `polls` polls
+ * (>= 1); the kernel then sets the filter's sticky timeout status and
+ * returns.  The next sbf_get_status reports SBF_ERR_CUDA ("a bounded device
+ * wait timed out") and clears the status; the filter is unchanged.  Every
+ * other launch uses the kernels' normal bound (about 2^22 polls).  Async on
+ * `stream`.  SBF_ERR_INVALID_ARG when polls < 1 or the filter's kernels are
+ * not the strip kernels (the only ones with bounded waits). */
+int sbf_test_wait_timeout(sbf_filter *f, int polls, void *stream);
+
 /* Synchronize `stream`, then return and clear the sticky device status:
  * SBF_OK, SBF_ERR_BAD_OFFSETS, or SBF_ERR_CUDA if the stream reported an
  * error. */

@@ -29,7 +29,8 @@ int sbf_probe_sm_count(int *sms);
 /* Integer instruction throughput.  kind: 0 = the mix that dominates the
  * filter kernels' ALU pipe (LOP3, funnel shift, compare, select, min: five
  * instructions per step), 1 = LOP3 only, 2 = funnel shift only, 3 = integer
- * multiply-add only (the FMA pipe).  Each of blocks x threads threads runs
+ * multiply-add only (the FMA pipe), 4 = 64-bit unsigned minimum (min.u64;
+ * three per step, counted as one operation each).  Each of blocks x threads threads runs
  * `iters` rounds of 32 steps over eight independent chains.  *ops receives the
  * instructions one launch executes (threads x iters x 32 x instructions per
  * step).  sink: device uint32[blocks * threads], written once per thread. */

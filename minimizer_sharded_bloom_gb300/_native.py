@@ -40,6 +40,7 @@ SIGNATURES = {
     "sbf_get_params": (_i32, [_vp, _ip, _ip, _ip, _ip, ctypes.POINTER(ctypes.c_uint64)]),
     "sbf_is_specialized": (_i32, [_vp]),
     "sbf_get_status": (_i32, [_vp, _vp]),
+    "sbf_test_wait_timeout": (_i32, [_vp, _i32, _vp]),
     "sbf_last_error": (ctypes.c_char_p, []),
     "sbf_fastx_open": (_vp, [ctypes.c_char_p]),
     "sbf_fastx_next": (_i64, [_vp, _vp, _i64, _vp, _i64, ctypes.POINTER(ctypes.c_int64)]),
@@ -200,6 +201,10 @@ def sbf_is_specialized(f: int) -> bool:
 
 def sbf_get_status(f: int, stream: int = 0) -> int:
     return int(load().sbf_get_status(f, stream))
+
+
+def sbf_test_wait_timeout(f: int, polls: int, stream: int = 0) -> None:
+    check(load().sbf_test_wait_timeout(f, polls, stream), "sbf_test_wait_timeout")
 
 
 def sbf_last_error() -> str:

@@ -148,6 +148,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.rec_len = 0;
     la.nonuniform = nullptr;
     la.out_words_end = INT64_MAX;
+    la.wait_test = 0;
     return la;
 }
 
@@ -305,6 +306,7 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     if (alphabet != SBF_ALPHABET_DNA && shards <= (1ull << 31) &&
         sbf::find_alphabet_strip(alphabet, k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
+        f->strip = true;
         threads_query = threads;
     } else if (alphabet != SBF_ALPHABET_DNA) {
         bool spec = false;
@@ -313,6 +315,7 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
         threads = 256;
     } else if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
+        f->strip = true;
     } else {
         ins = sbf::generic_insert_kernel();
         qry = sbf::generic_query_kernel();
@@ -442,6 +445,15 @@ int sbf_clear(sbf_filter *f, void *stream) {
     if (!f) return fail(SBF_ERR_INVALID_ARG, "NULL filter");
     cudaError_t e = cudaMemsetAsync(f->words, 0, f->num_shards * 32, as_stream(stream));
     return e == cudaSuccess ? SBF_OK : cuda_fail(e, "sbf_clear");
+}
+
+int sbf_test_wait_timeout(sbf_filter *f, int polls, void *stream) {
+    if (!f || polls < 1) return fail(SBF_ERR_INVALID_ARG, "sbf_test_wait_timeout: bad arguments");
+    if (!f->strip) return fail(SBF_ERR_INVALID_ARG, "sbf_test_wait_timeout: the filter's kernels have no bounded waits");
+    if (int rc = check_device(f)) return rc;
+    sbf::LaunchArgs la = make_args(f, nullptr, nullptr, 0, nullptr);
+    la.wait_test = polls;
+    return launch(f->insert_kernel, 1, f->threads, la, as_stream(stream));
 }
 
 int sbf_get_status(sbf_filter *f, void *stream) {

@@ -36,6 +36,10 @@ struct LaunchArgs {
                               // offsets check saw records of different lengths (else nullptr)
     int64_t out_words_end;    // query: answer words at or past this index are not written
                               // (a chunk of a larger batch cut inside a record); else INT64_MAX
+    int wait_test;            // failure-detection test: > 0 = before any work, one thread waits
+                              // on an mbarrier that nothing completes, giving up after
+                              // wait_test polls; the kernel then reports the timeout and
+                              // returns (no copy is in flight).  0 in every normal launch.
 };
 
 // Minimizer hash (Sec. IV-G, minimizer role): one multiplicative mix, then an

@@ -26,6 +26,7 @@ struct sbf_filter {
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
     bool specialized = false;
+    bool strip = false;         // insert/query kernels are strip kernels (bounded mbarrier waits)
     void *stager = nullptr;     // host-facing staging buffers, created on first use
     int64_t host_chunk = int64_t(1) << 26;  // host-facing chunk, in positions
     int host_mode = 0;          // 0: read host buffers in place when possible; 1: always stage

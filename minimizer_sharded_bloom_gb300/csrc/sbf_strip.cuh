@@ -27,9 +27,9 @@
 //  * Two passes per block of w k-mers: pass A (minimizer front) produces the
 //    w shards of the block, pass B (s-mer front) hashes the s-mers, builds each
 //    k-mer's four word masks and inserts or tests them.  For query, pass A
-//    issues an L1 prefetch of each new shard, so the 32-byte shard is on chip
-//    by the time pass B reads it (Sec. IV-E/IV-G: one 256-bit non-coherent
-//    load per shard).
+//    copies each run head's 32-byte shard into shared memory (cp.async), so
+//    the shard is on chip by the time pass B reads it (Sec. IV-E/IV-G: one
+//    256-bit load per shard).
 //
 //  * Runs (Fig. 3): consecutive k-mers of a strip with one shard form a run;
 //    their masks are ORed in registers and the run issues one 64-bit atomic OR
@@ -113,10 +113,54 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
     }
 }
 
-// One 256-bit shard through the non-coherent path (Sec. IV-G).
+// Per-warp queue of finished runs (DNA insert).  A lane whose run ends
+// writes it (shard key, eight half-words) at the queue's tail; once
+// drain_at runs wait, the warp drains them in groups of eight, lane l
+// reducing word l & 3 of run l >> 2, so that each run's four words reach L2
+// as one 32-byte request instead of four (drain_at = 1: drain everything,
+// the last group partly).  head / tail are warp-uniform counters; the ring
+// holds QN = 64 entries (with drain_at <= 32, at most 31 wait after a drain
+// and a step adds at most 32).  Called by all 32 lanes.
+template <int H, int QN>
+__device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int &head, int &tail, bool flush,
+                                           uint32_t key, const uint32_t acc[8], int lane, int drain_at,
+                                           uint64_t *words) {
+    const unsigned fm = __ballot_sync(0xffffffffu, flush);
+    if (fm) {
+        if (flush) {
+            const int e = (tail + __popc(fm & ((1u << lane) - 1u))) & (QN - 1);
+            q_key[e] = key;
+            uint4 *d = reinterpret_cast<uint4 *>(q_acc + 8 * e);
+            d[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+            d[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        tail += __popc(fm);
+    }
+    if (tail - head >= drain_at) {
+        __syncwarp();
+        const int wd = lane & 3;
+        do {
+            if (head + (lane >> 2) < tail) {
+                const int e = (head + (lane >> 2)) & (QN - 1);
+                const uint2 v = reinterpret_cast<const uint2 *>(q_acc + 8 * e)[wd];
+                const uint64_t x = ((uint64_t)v.y << 32) | v.x;
+                if (wd < H && x)
+                    asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)q_key[e] * 4 + wd), "l"(x)
+                                 : "memory");
+            }
+            head += 8;
+        } while (tail - head >= (drain_at > 1 ? 8 : 1));
+        if (head > tail) head = tail;
+        __syncwarp();
+    }
+}
+
+// One 256-bit shard through the non-coherent path (Sec. IV-G).  The L2
+// fetches 64 bytes around it instead of its default 128-byte line: scattered
+// shards gain nothing from the larger fetch (same rate, twice the DRAM bytes).
 __device__ __forceinline__ void load_shard(const uint64_t *p, uint64_t &a, uint64_t &b, uint64_t &c,
                                            uint64_t &d) {
-    asm volatile("ld.global.nc.v4.u64 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L2::64B.v4.u64 {%0, %1, %2, %3}, [%4];"
                  : "=l"(a), "=l"(b), "=l"(c), "=l"(d)
                  : "l"(p));
 }
@@ -231,6 +275,16 @@ __device__ __forceinline__ uint32_t keep_if(uint32_t x, uint32_t b) {
 }
 
 
+// 16-byte asynchronous global -> shared copy through L2 only; the L2 fetches
+// the 64 bytes around it rather than a 128-byte line (scattered shards: same
+// rate, half the DRAM bytes).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global.L2::64B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -256,9 +310,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
                  : "memory");
     return ok != 0;
 }
-// Bounded wait: false after ~2^22 polls (the copy never completed).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    for (int it = 0; it < (1 << 22); ++it)
+// Bounded wait: false after `polls` polls (by default ~2^22: the copy never
+// completed).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int polls = 1 << 22) {
+    for (int it = 0; it < polls; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -267,14 +322,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
-
-// 16-byte asynchronous global -> shared copy through L2 only.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int K_, int M_, int S_, int H_, int A_ = 0, int D_ = 0>
 struct StripCfg {
@@ -377,8 +424,24 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
     __shared__ StripSmem<K, M, S, H, A, D> sm;
     // query: shards of the current block's run heads, [slot][half][thread]
     __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
+    // DNA insert: per warp, a ring of finished runs (shard key, eight
+    // half-words) that the warp drains four lanes per run
+    constexpr bool kQueue = !kQuery && A == 0;
+    constexpr int QN = 64;
+    __shared__ __align__(16) uint32_t fq_acc[kQueue ? (NT / 32) * QN * 8 : 1];
+    __shared__ uint32_t fq_key[kQueue ? (NT / 32) * QN : 1];
 
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
+    if (a.wait_test > 0) {
+        // failure-detection test: a bounded wait that cannot succeed (an
+        // mbarrier with one expected arrival that never comes, no copy
+        // attached) gives up and is reported as the sticky timeout status
+        if (threadIdx.x == 0) {
+            mbar_init(&sm.raw_bar, 1);
+            if (!mbar_wait(&sm.raw_bar, 0, a.wait_test)) atomicOr(a.status, kStatusTimeout);
+        }
+        return;
+    }
     // dense batches: record r is bytes [r rlen, (r + 1) rlen), a tile holds NT
     // records; the geometry below is runtime there and the constants otherwise.
     // A CSR batch runs dense too when the offsets check found every record of
@@ -418,6 +481,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         mbar_init(&sm.raw_bar, 1);
         sm.abort_flag = 0;
     }
+
     if (kQuery && tid < 64)
         sm.onehot[tid] = make_uint2(tid < 32 ? 1u << tid : 0u, tid >= 32 ? 1u << (tid - 32) : 0u);
     __syncthreads();
@@ -720,6 +784,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
             for (int j = 0; j < 8; ++j) acc[j] = 0u;
             uint64_t F0 = 0, F1 = 0, F2 = 0, F3 = 0;
             uint64_t *const words = a.words;
+            int q_head = 0, q_tail = 0;  // DNA insert: the warp's run queue (warp-uniform)
 
 #pragma unroll 1
             for (int blk = 0; blk <= nbl; ++blk) {
@@ -730,6 +795,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                 int nh = 0;
                 uint32_t heads = 0;
                 const uint32_t last_before = shard[W - 1];
+
                 const int kb = kk0 + (blk - 1) * W;
                 uint64_t vwin = 0;
                 if (blk > 0) vwin = bits64_at(sm.valid, kb);
@@ -823,7 +889,12 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             // DNA (runs of ~(w+1)/2 = 8.5 k-mers): each lane flushes its own
                             // runs; protein (runs of ~3): the warp flushes cooperatively
                             if constexpr (A == 0) {
-                                if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                                const bool fl = key != cur_key && !(cur_key >> 31);
+                                if (am == 0xffffffffu)
+                                    queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head,
+                                                      q_tail, fl, cur_key, acc, tid & 31, 8, words);
+                                else if (fl)
+                                    flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                             } else {
                                 flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am);
                             }
@@ -872,7 +943,12 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
             }
             if constexpr (!kQuery) {
                 if constexpr (A == 0) {
-                    if (!(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                    // the strip's last runs, then everything still queued
+                    if (am == 0xffffffffu)
+                        queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head, q_tail,
+                                          !(cur_key >> 31), cur_key, acc, tid & 31, 1, words);
+                    else if (!(cur_key >> 31))
+                        flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                 } else {
                     flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am);
                 }

@@ -19,7 +19,7 @@ from . import build_lib
 _lock = threading.Lock()
 _lib = None
 
-ALU_KINDS = {"mix": 0, "lop3": 1, "shf": 2, "imad": 3}
+ALU_KINDS = {"mix": 0, "lop3": 1, "shf": 2, "imad": 3, "min64": 4}
 RMW_MODES = {"red4": 0, "red_lanes": 1, "ld_st": 2, "red_queue": 3}
 READ_MODES = {"ld_nc": 0, "ld_nc_L2_64B": 1, "ld_nc_L2_128B": 2, "ld_nc_L2_256B": 3,
               "cp_async": 4, "cp_async_L2_64B": 5, "bulk32": 6}

@@ -43,10 +43,18 @@ __device__ __forceinline__ void alu_step(uint32_t &x, uint32_t &y, uint32_t &z) 
         asm volatile("shf.l.wrap.b32 %0, %0, %1, 5;" : "+r"(x) : "r"(y));
         asm volatile("shf.l.wrap.b32 %0, %0, %1, 11;" : "+r"(y) : "r"(z));
         asm volatile("shf.l.wrap.b32 %0, %0, %1, 17;" : "+r"(z) : "r"(x));
-    } else {
+    } else if constexpr (KIND == 3) {
         asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(x) : "r"(y), "r"(z));
         asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(y) : "r"(z), "r"(x));
         asm volatile("mad.lo.u32 %0, %0, %1, %2;" : "+r"(z) : "r"(x), "r"(y));
+    } else {
+        // 64-bit unsigned minimum of (x:y) and (z:x), three per step
+        asm volatile("{ .reg .b64 a, b; mov.b64 a, {%0, %1}; mov.b64 b, {%2, %0}; min.u64 a, a, b;"
+                     " mov.b64 {%0, %1}, a; }" : "+r"(x), "+r"(y) : "r"(z));
+        asm volatile("{ .reg .b64 a, b; mov.b64 a, {%0, %1}; mov.b64 b, {%2, %1}; min.u64 a, a, b;"
+                     " mov.b64 {%0, %1}, a; }" : "+r"(y), "+r"(z) : "r"(x));
+        asm volatile("{ .reg .b64 a, b; mov.b64 a, {%0, %1}; mov.b64 b, {%1, %2}; min.u64 a, a, b;"
+                     " mov.b64 {%0, %1}, a; }" : "+r"(z), "+r"(x) : "r"(y));
     }
 }
 
@@ -286,13 +294,14 @@ int sbf_probe_sm_count(int *sms) {
 }
 
 int sbf_probe_alu(int kind, int iters, int blocks, int threads, uint32_t *sink, void *stream, double *ops) {
-    if (kind < 0 || kind > 3 || iters < 1 || blocks < 1 || threads < 32 || threads > 1024 || !sink) return -1;
+    if (kind < 0 || kind > 4 || iters < 1 || blocks < 1 || threads < 32 || threads > 1024 || !sink) return -1;
     cudaStream_t st = as_stream(stream);
     switch (kind) {
         case 0: probe_alu_kernel<0><<<blocks, threads, 0, st>>>(iters, sink); break;
         case 1: probe_alu_kernel<1><<<blocks, threads, 0, st>>>(iters, sink); break;
         case 2: probe_alu_kernel<2><<<blocks, threads, 0, st>>>(iters, sink); break;
-        default: probe_alu_kernel<3><<<blocks, threads, 0, st>>>(iters, sink); break;
+        case 3: probe_alu_kernel<3><<<blocks, threads, 0, st>>>(iters, sink); break;
+        default: probe_alu_kernel<4><<<blocks, threads, 0, st>>>(iters, sink); break;
     }
     if (ops)
         *ops = (double)blocks * threads * (double)iters * kAluSteps * kAluChains * alu_ops_per_step(kind);

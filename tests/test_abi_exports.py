@@ -69,6 +69,7 @@ def test_argument_errors_need_no_gpu(lib):
     assert L.sbf_insert(None, None, None, 1, None) == _native.SBF_ERR_INVALID_ARG
     assert L.sbf_query(None, None, None, 1, None, None) == _native.SBF_ERR_INVALID_ARG
     assert L.sbf_num_shards(None) == 0
+    assert L.sbf_test_wait_timeout(None, 1, None) == _native.SBF_ERR_INVALID_ARG
     L.sbf_destroy(None)
 
 
