@@ -787,8 +787,8 @@ def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps, "ms_per_step": 1e3 * med, "ms_per_step_mean": 1e3 * mean,
             "ms_per_step_max": 1e3 * worst, "value_from_mean": throughput(world, 1, nk_total, mean),
-            "insert_host_ms": {"median": ms[0], "max": ms[1]},
-            "query_host_ms": {"median": ms[2], "max": ms[3]},
+            "insert_host_ms": {"median": ms[0], "max": ms[1], "all": [round(1e3 * x, 3) for x in ti]},
+            "query_host_ms": {"median": ms[2], "max": ms[3], "all": [round(1e3 * x, 3) for x in tq]},
             "link_h2d_gbs": statistics.median(link),
             "link_bound_ms_per_step": 1e3 * h2d / (statistics.median(link) * 1e9),
             "path": "sbf_insert_host + sbf_query_host, pinned host buffers, host clock per call; "

@@ -13,12 +13,14 @@
 // clipped at a chunk's start keeps its symbol frame (DNA triplets).  The
 // kernels index absolute positions: a chunk's offsets are the caller's, as
 // they are, with both ends clipped, and its staged bytes are addressed through
-// a pointer biased by cs, so the host never rewrites the offsets.  Chunk c
-// runs on slot c mod 4 (a stream, device buffers and pinned buffers, all kept in
-// the filter between calls); the host prepares chunk c+1 while the GPU works
-// on chunk c.  Host buffers that are already page-locked are copied from
+// a pointer biased by cs, so the host never rewrites the offsets (a chunk's
+// two clipped ends are written on the device).  Chunk c runs on slot c mod 4
+// (a stream, device buffers and pinned buffers, all kept in the filter
+// between calls).  Host buffers that are already page-locked are copied from
 // directly; pageable ones go through the pinned staging buffers.  Answers go
-// straight to the caller's buffer where the device can write it.
+// straight to the caller's buffer where the device can write it.  When no
+// pinned staging buffer is in play, every chunk is enqueued at once and the
+// host waits once; otherwise it waits for a slot before reusing its buffers.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -90,6 +92,18 @@ cudaError_t prepare(Slot &s, int64_t seq_bytes, int64_t n_off, int64_t n_off_hos
     if (e == cudaSuccess) e = grow_pinned(s.h_off, s.cap_hoff, std::max<int64_t>(n_off_host, 2));
     if (e == cudaSuccess && stage_out) e = grow_pinned(s.h_out, s.cap_hout, out_words);
     return e;
+}
+
+// The two clipped ends of a chunk's device offsets, written on the device so
+// that no host buffer has to outlive the call's enqueueing.
+__global__ void patch_ends_kernel(int64_t *off, int64_t n_loc, int64_t first, int64_t last) {
+    if (threadIdx.x == 0) off[0] = first;
+    if (threadIdx.x == 1) off[n_loc] = last;
+}
+
+cudaError_t patch_ends(int64_t *off, int64_t n_loc, int64_t first, int64_t last, cudaStream_t st) {
+    patch_ends_kernel<<<1, 32, 0, st>>>(off, n_loc, first, last);
+    return cudaGetLastError();
 }
 
 // 1 = page-locked host memory, 0 = pageable host memory, -1 = not host memory.
@@ -243,6 +257,14 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     }
     cudaEventRecord(checked, reinterpret_cast<cudaStream_t>(user_stream));
 
+    // With page-locked input, offsets the device reads whole or page-locked,
+    // and answers the device writes in place, no host buffer is reused from
+    // chunk to chunk: every chunk is enqueued at once (a slot's stream orders
+    // its device buffers) and the host waits once at the end, so a host
+    // thread that is descheduled mid-call does not leave the GPU idle.
+    // Otherwise a slot's pinned staging buffers are reused four chunks on,
+    // after a wait for that slot.
+    const bool host_staging = seq_kind == 0 || (query && !out_dev) || (!all_off && !off_pinned);
     const int64_t kb = sbf::kmer_bytes(f);
     // the chunks and their clipped ends (sbf_chunks.h); a query's chunks also
     // shrink towards the batch's end, an insert's do not (its kernels take
@@ -250,6 +272,16 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
     // throughput)
     sbf::ChunkPlan plan(off, n, f->host_chunk, kb, sbf::symbol_bytes(f->alphabet), query);
     const int64_t chunk_max = plan.chunk_max();
+    // the most records any chunk holds: every slot's offsets buffer is sized
+    // for it before the first chunk, so no buffer grows (and frees) while
+    // earlier chunks are in flight (plain host arithmetic over the plan)
+    int64_t max_recs = 1;
+    {
+        sbf::ChunkPlan pre(off, n, f->host_chunk, sbf::kmer_bytes(f), sbf::symbol_bytes(f->alphabet), query);
+        sbf::Chunk c0;
+        while (pre.next(c0))
+            if (!c0.empty) max_recs = std::max<int64_t>(max_recs, c0.r1 - c0.r0);
+    }
     int rc = SBF_OK;
     sbf::Chunk ch;
     for (int64_t c = 0; rc == SBF_OK && plan.next(ch); ++c) {
@@ -260,7 +292,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel may write
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
         Slot &s = st.slot[c % 4];
-        if (s.stream) {
+        if (s.stream && host_staging) {
             if (cudaStreamSynchronize(s.stream) != cudaSuccess) {
                 rc = set_error(SBF_ERR_CUDA, "staging stream failed");
                 break;
@@ -272,7 +304,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         // sized for the largest chunk at once: growing a buffer mid-call would
         // free it, which waits for the whole device
         const int64_t max_bytes = std::max<int64_t>(data_hi - cs, chunk_max + kb);
-        if (prepare(s, max_bytes, n_loc + 1, off_pinned ? 2 : n_loc + 1,
+        if (prepare(s, max_bytes, max_recs + 1, (all_off || off_pinned) ? 2 : max_recs + 1,
                     stage_out ? std::max<int64_t>(dev_words, (max_bytes + 31) / 32 + 1) : 0, seq_kind == 0,
                     stage_out) != cudaSuccess) {
             cudaGetLastError();
@@ -297,22 +329,14 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
             if (whole) {
                 k_off = st.d_all_off + r0;
             } else {
-                s.h_off[0] = first;
-                s.h_off[1] = last;
                 if (e == cudaSuccess)
                     e = cudaMemcpyAsync(s.d_off, st.d_all_off + r0, off_bytes, cudaMemcpyDeviceToDevice, s.stream);
-                if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, s.h_off, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
-                if (e == cudaSuccess)
-                    e = cudaMemcpyAsync(s.d_off + n_loc, s.h_off + 1, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+                if (e == cudaSuccess) e = patch_ends(s.d_off, n_loc, first, last, s.stream);
             }
         } else if (off_pinned) {
             // the slice straight from the caller's page-locked array, then the two ends
-            s.h_off[0] = first;
-            s.h_off[1] = last;
             if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, off + r0, off_bytes, cudaMemcpyHostToDevice, s.stream);
-            if (e == cudaSuccess) e = cudaMemcpyAsync(s.d_off, s.h_off, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(s.d_off + n_loc, s.h_off + 1, sizeof(int64_t), cudaMemcpyHostToDevice, s.stream);
+            if (e == cudaSuccess) e = patch_ends(s.d_off, n_loc, first, last, s.stream);
         } else {
             std::memcpy(s.h_off, off + r0, off_bytes);
             s.h_off[0] = first;
