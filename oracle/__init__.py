@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.orc_salt.restype = u64
             L.orc_smer_bits.argtypes = [u64, i32, vp]
             L.orc_smer_bits.restype = None
+            L.orc_smer_bits_sectors.argtypes = [u64, i32, i32, vp]
+            L.orc_smer_bits_sectors.restype = None
             L.orc_symbol_bits.argtypes = [i32]
             L.orc_symbol_bits.restype = i32
             L.orc_symbol_bytes.argtypes = [i32]
@@ -74,18 +76,18 @@ def lib() -> ctypes.CDLL:
             L.orc_symbol_code.restype = i32
             L.orc_pack_symbols.argtypes = [i32, ctypes.c_char_p, i32]
             L.orc_pack_symbols.restype = u64
-            L.orc_insert.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32]
+            L.orc_insert.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32, i32]
             L.orc_insert.restype = i32
-            L.orc_query.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, vp, i32]
+            L.orc_query.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32, vp, i32]
             L.orc_query.restype = i32
-            L.orc_kmer_info.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, u64, u64, i32, vp, vp]
+            L.orc_kmer_info.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, u64, u64, i32, i32, vp, vp]
             L.orc_kmer_info.restype = i32
-            L.orc_count_runs.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, vp, vp, vp]
+            L.orc_count_runs.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32, vp, vp, vp]
             L.orc_count_runs.restype = i32
-            L.orc_kmer_batch.argtypes = [vp, vp, i64, vp, i64, i32, i32, i32, i32, u64, u64, i32,
+            L.orc_kmer_batch.argtypes = [vp, vp, i64, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32,
                                          vp, vp, vp]
             L.orc_kmer_batch.restype = i32
-            L.orc_kmer_rows.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, vp, vp, vp]
+            L.orc_kmer_rows.argtypes = [vp, vp, i64, i32, i32, i32, i32, u64, u64, i32, i32, vp, vp, vp]
             L.orc_kmer_rows.restype = i32
             _lib = L
     return _lib
@@ -136,14 +138,15 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def insert(filter_words: np.ndarray, seq, offsets, k, m, s, H, seed, nthreads=1,
-           alphabet=DNA) -> np.ndarray:
+           alphabet=DNA, sectors=0) -> np.ndarray:
     """OR every valid k-mer of every record into filter_words (uint64[S, 4]),
-    in place, and return it."""
+    in place, and return it.  sectors = 1: hash-chosen words for H < 4 (see
+    smer_bits)."""
     F = filter_words
     assert F.dtype == np.uint64 and F.ndim == 2 and F.shape[1] == 4 and F.flags.c_contiguous
     a, o = _u8(seq), _i64(offsets)
     rc = lib().orc_insert(_ptr(F), _ptr(a), _ptr(o), o.size - 1, k, m, s, H,
-                          F.shape[0], seed & (2**64 - 1), alphabet_id(alphabet), nthreads)
+                          F.shape[0], seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), nthreads)
     if rc != 0:
         raise ValueError("orc_insert rejected its arguments")
     return F
@@ -154,7 +157,7 @@ def new_filter(num_bits: int) -> np.ndarray:
 
 
 def query(filter_words: np.ndarray, seq, offsets, k, m, s, H, seed, nthreads=1,
-          alphabet=DNA) -> np.ndarray:
+          alphabet=DNA, sectors=0) -> np.ndarray:
     """Answer bits for every absolute position of [offsets[0], offsets[-1]).
 
     Returns uint32[(offsets[-1] + 31) // 32]; words below offsets[0] >> 5 stay
@@ -164,32 +167,34 @@ def query(filter_words: np.ndarray, seq, offsets, k, m, s, H, seed, nthreads=1,
     a, o = _u8(seq), _i64(offsets)
     out = np.zeros(max(1, (int(o[-1]) + 31) // 32), dtype=np.uint32)
     rc = lib().orc_query(_ptr(F), _ptr(a), _ptr(o), o.size - 1, k, m, s, H,
-                         F.shape[0], seed & (2**64 - 1), alphabet_id(alphabet), _ptr(out), nthreads)
+                         F.shape[0], seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), _ptr(out),
+                         nthreads)
     if rc != 0:
         raise ValueError("orc_query rejected its arguments")
     return out
 
 
-def kmer_info(seq, offsets, g, k, m, s, H, num_shards, seed, alphabet=DNA):
+def kmer_info(seq, offsets, g, k, m, s, H, num_shards, seed, alphabet=DNA, sectors=0):
     """(valid, shard, K[4]) for the k-mer at absolute position g."""
     a, o = _u8(seq), _i64(offsets)
     shard = np.zeros(1, dtype=np.uint64)
     K = np.zeros(4, dtype=np.uint64)
     rc = lib().orc_kmer_info(_ptr(a), _ptr(o), o.size - 1, int(g), k, m, s, H,
-                             num_shards, seed & (2**64 - 1), alphabet_id(alphabet), _ptr(shard), _ptr(K))
+                             num_shards, seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), _ptr(shard),
+                             _ptr(K))
     if rc < 0:
         raise ValueError("orc_kmer_info rejected its arguments")
     return bool(rc), int(shard[0]), [int(x) for x in K]
 
 
-def count_runs(seq, offsets, k, m, s, H, num_shards, seed, alphabet=DNA):
+def count_runs(seq, offsets, k, m, s, H, num_shards, seed, alphabet=DNA, sectors=0):
     """(valid k-mers, runs, atomics): runs are maximal stretches of consecutive
     valid k-mers of one record sharing a shard (Fig. 3); atomics counts the
     non-zero words over all runs."""
     a, o = _u8(seq), _i64(offsets)
     res = np.zeros(3, dtype=np.int64)
     rc = lib().orc_count_runs(_ptr(a), _ptr(o), o.size - 1, k, m, s, H, num_shards,
-                              seed & (2**64 - 1), alphabet_id(alphabet), _ptr(res[0:]), _ptr(res[1:]),
+                              seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), _ptr(res[0:]), _ptr(res[1:]),
                               _ptr(res[2:]))
     if rc != 0:
         raise ValueError("orc_count_runs rejected its arguments")
@@ -223,9 +228,12 @@ def symbol_bits(alphabet) -> int:
     return int(lib().orc_symbol_bits(alphabet_id(alphabet)))
 
 
-def smer_bits(hs: int, H: int):
+def smer_bits(hs: int, H: int, sectors: int = 0):
+    """The four word masks of one s-mer hash (Sec. IV-B, IV-G); sectors = 1
+    puts hash i of an H < 4 filter in the word given by the two slice bits
+    above its position bits instead of word i mod 4."""
     w = np.zeros(4, dtype=np.uint64)
-    lib().orc_smer_bits(hs & (2**64 - 1), H, _ptr(w))
+    lib().orc_smer_bits_sectors(hs & (2**64 - 1), H, int(sectors), _ptr(w))
     return [int(x) for x in w]
 
 
@@ -234,7 +242,7 @@ def constants():
     return int(L.orc_const_c1()), int(L.orc_const_c2())
 
 
-def kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet=DNA):
+def kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet=DNA, sectors=0):
     """(valid[bool], shard[uint64], K[uint64, 4]) for each absolute position."""
     a, o = _u8(seq), _i64(offsets)
     pos = np.ascontiguousarray(positions, dtype=np.int64)
@@ -243,20 +251,20 @@ def kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet=D
     K = np.zeros((pos.size, 4), dtype=np.uint64)
     if pos.size:
         rc = lib().orc_kmer_batch(_ptr(a), _ptr(o), o.size - 1, _ptr(pos), pos.size, k, m, s, H,
-                                  num_shards, seed & (2**64 - 1), alphabet_id(alphabet), _ptr(valid),
+                                  num_shards, seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), _ptr(valid),
                                   _ptr(shard), _ptr(K))
         if rc != 0:
             raise ValueError("orc_kmer_batch rejected its arguments")
     return valid.astype(bool), shard, K
 
 
-def query_sampled(shard_words, seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet=DNA):
+def query_sampled(shard_words, seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet=DNA, sectors=0):
     """Answers for selected absolute positions only, for filters too large to
     copy whole.  shard_words(uint64 array of shards) -> uint64[len, 4] supplies
     the image words of the requested shards.  Each answer follows Algorithm 2:
     present iff the k-mer is valid and every bit of its s-mers is set in its
     shard."""
-    valid, shard, K = kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet)
+    valid, shard, K = kmer_batch(seq, offsets, positions, k, m, s, H, num_shards, seed, alphabet, sectors)
     out = np.zeros(valid.size, dtype=bool)
     if valid.any():
         F = np.asarray(shard_words(shard[valid]), dtype=np.uint64).reshape(-1, 4)
@@ -264,7 +272,7 @@ def query_sampled(shard_words, seq, offsets, positions, k, m, s, H, num_shards, 
     return out
 
 
-def insert_sparse(seq, offsets, k, m, s, H, num_shards, seed, alphabet=DNA):
+def insert_sparse(seq, offsets, k, m, s, H, num_shards, seed, alphabet=DNA, sectors=0):
     """The image a full insert produces, as (sorted non-zero shard indices,
     uint64[len, 4] words), without allocating num_shards rows: every valid
     k-mer's (shard, K) from scratch, then an OR per shard (a sort and a
@@ -275,7 +283,8 @@ def insert_sparse(seq, offsets, k, m, s, H, num_shards, seed, alphabet=DNA):
     K = np.zeros((max(total, 1), 4), dtype=np.uint64)
     cnt = np.zeros(1, dtype=np.int64)
     rc = lib().orc_kmer_rows(_ptr(a), _ptr(o), o.size - 1, k, m, s, H, num_shards,
-                             seed & (2**64 - 1), alphabet_id(alphabet), _ptr(shard), _ptr(K), _ptr(cnt))
+                             seed & (2**64 - 1), alphabet_id(alphabet), int(sectors), _ptr(shard), _ptr(K),
+                             _ptr(cnt))
     if rc != 0:
         raise ValueError("orc_kmer_rows rejected its arguments")
     c = int(cnt[0])

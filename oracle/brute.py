@@ -78,9 +78,11 @@ def salt(i: int) -> int:
     return z | 1
 
 
-def smer_words(h: int, H: int):
+def smer_words(h: int, H: int, sectors: int = 0):
     """Bit i: the low 6 bits of slice i while slices are >= 6 bits wide,
-    otherwise the top 6 bits of h * salt(i) mod 2^64."""
+    otherwise the top 6 bits of h * salt(i) mod 2^64; in word i mod 4, or,
+    with sectors = 1 and H < 4, in the word numbered by the two bits of slice
+    i that follow its six position bits."""
     words = [0, 0, 0, 0]
     width = 64 // H
     for i in range(H):
@@ -88,12 +90,15 @@ def smer_words(h: int, H: int):
             pos = (h >> (i * width)) & 63
         else:
             pos = ((h * salt(i)) & MASK64) >> 58
-        words[i % 4] |= 1 << pos
+        word = i % 4
+        if sectors and H < 4:
+            word = (h >> (i * width + 6)) & 3
+        words[word] |= 1 << pos
     return words
 
 
 def kmer(text: str, k: int, m: int, s: int, H: int, num_shards: int, seed: int,
-         alphabet: str = "dna"):
+         alphabet: str = "dna", sectors: int = 0):
     """(shard, words) of one valid k-mer given as its k symbols' characters."""
     _, cw = _SHAPE[alphabet]
     minimizer = min(hm(kmer_value(text[cw * i:cw * (i + m)], alphabet), seed)
@@ -101,7 +106,7 @@ def kmer(text: str, k: int, m: int, s: int, H: int, num_shards: int, seed: int,
     shard = minimizer % num_shards
     words = [0, 0, 0, 0]
     for j in range(k - s + 1):
-        for w, bits in enumerate(smer_words(hs(kmer_value(text[cw * j:cw * (j + s)], alphabet), seed), H)):
+        for w, bits in enumerate(smer_words(hs(kmer_value(text[cw * j:cw * (j + s)], alphabet), seed), H, sectors)):
             words[w] |= bits
     return shard, words
 
@@ -119,28 +124,30 @@ def kmers_of(rec: str, k: int, alphabet: str = "dna"):
         yield p, rec[p:p + cw * k]
 
 
-def insert(seq: bytes, offsets, k, m, s, H, num_shards, seed, filt=None, alphabet: str = "dna"):
+def insert(seq: bytes, offsets, k, m, s, H, num_shards, seed, filt=None, alphabet: str = "dna",
+           sectors: int = 0):
     """Return {shard: [w0, w1, w2, w3]} with every valid k-mer inserted."""
     filt = {} if filt is None else filt
     for _, rec in records_of(seq, offsets):
         for p, text in kmers_of(rec, k, alphabet):
             if not is_valid(text, alphabet):
                 continue
-            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet)
+            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet, sectors)
             cur = filt.setdefault(shard, [0, 0, 0, 0])
             for w in range(4):
                 cur[w] |= words[w]
     return filt
 
 
-def query(filt, seq: bytes, offsets, k, m, s, H, num_shards, seed, alphabet: str = "dna"):
+def query(filt, seq: bytes, offsets, k, m, s, H, num_shards, seed, alphabet: str = "dna",
+          sectors: int = 0):
     """Return the set of absolute positions whose k-mer answers present."""
     hits = set()
     for start, rec in records_of(seq, offsets):
         for p, text in kmers_of(rec, k, alphabet):
             if not is_valid(text, alphabet):
                 continue
-            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet)
+            shard, words = kmer(text, k, m, s, H, num_shards, seed, alphabet, sectors)
             have = filt.get(shard, [0, 0, 0, 0])
             if all((words[w] & ~have[w]) == 0 for w in range(4)):
                 hits.add(start + p)

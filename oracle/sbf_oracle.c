@@ -49,6 +49,11 @@
  *     (hs >> (i*W)) & 63, in word i mod 4, while W >= 6 (H <= 10); for
  *     11 <= H <= 32, position = top 6 bits of hs * salt(i) mod 2^64, salt(i)
  *     = SplitMix64 output i from state 0 (golden-ratio increment), made odd;
+ *   - optional hash-chosen sectors (sectors = 1, an extension, not the
+ *     paper's layout): for H < 4, where "i mod 4" leaves words H..3 of every
+ *     shard empty, hash i goes to word (hs >> (i*W + 6)) & 3 -- the two bits
+ *     of slice i just above its position bits (W >= 21 there); H >= 4 keeps
+ *     word i mod 4;
  *   - records are given as CSR offsets; a k-mer never spans two records;
  *   - the minimum's tie-break is the leftmost window (it cannot change the
  *     result: hm is a bijection, equal hashes mean equal m-mers).
@@ -168,8 +173,10 @@ uint64_t orc_salt(int i)
  * Bit-slicing while a slice is at least 6 bits wide (64/H >= 6): the position
  * is the low 6 bits of slice i (slice width floor(64/H)).  For larger H the
  * paper multiplies by a per-index golden-ratio-derived salt and keeps the
- * upper bits: position = top 6 bits of hs * salt(i) mod 2^64. */
-void orc_smer_bits(uint64_t hs, int H, uint64_t words[4])
+ * upper bits: position = top 6 bits of hs * salt(i) mod 2^64.
+ * sectors = 1 (hash-chosen sectors, H < 4 only): hash i's word is the two
+ * bits of slice i above its six position bits instead of i mod 4. */
+void orc_smer_bits_sectors(uint64_t hs, int H, int sectors, uint64_t words[4])
 {
     int W = 64 / H;
     for (int i = 0; i < H; i++) {
@@ -178,8 +185,16 @@ void orc_smer_bits(uint64_t hs, int H, uint64_t words[4])
             pos = (int)((hs >> (i * W)) & 63u);
         else
             pos = (int)((hs * orc_salt(i)) >> 58);
-        words[i % 4] |= (uint64_t)1 << pos;
+        int word = i % 4;
+        if (sectors && H < 4)
+            word = (int)((hs >> (i * W + 6)) & 3u);
+        words[word] |= (uint64_t)1 << pos;
     }
+}
+
+void orc_smer_bits(uint64_t hs, int H, uint64_t words[4])
+{
+    orc_smer_bits_sectors(hs, H, 0, words);
 }
 
 typedef struct {
@@ -187,6 +202,7 @@ typedef struct {
     uint64_t num_shards; /* a power of two */
     uint64_t seed;
     int alphabet;
+    int sectors;         /* 0: hash i in word i mod 4; 1: hash-chosen words for H < 4 */
 } orc_params;
 
 /* One k-mer, from scratch.  seq is the whole concatenated buffer, g an
@@ -217,7 +233,8 @@ static int kmer_info(const uint8_t *seq, int64_t g, int64_t rec_start, int64_t r
     /* ... and the bits of all k-s+1 s-mers are OR-ed into four word masks. */
     K[0] = K[1] = K[2] = K[3] = 0;
     for (int j = 0; j <= k - s; j++)
-        orc_smer_bits(orc_hash_s(orc_pack_symbols(A, seq + g + (int64_t)B * j, s), ~P->seed), P->H, K);
+        orc_smer_bits_sectors(orc_hash_s(orc_pack_symbols(A, seq + g + (int64_t)B * j, s), ~P->seed), P->H,
+                              P->sectors, K);
     return 1;
 }
 
@@ -302,7 +319,7 @@ static int valid_params(const orc_params *P)
     if (P->k < 1 || P->k * orc_symbol_bits(P->alphabet) > 64 || P->m < 1 || P->m > P->k ||
         P->s < 1 || P->s > P->k)
         return 0;
-    if (P->H < 1 || P->H > 32)
+    if (P->H < 1 || P->H > 32 || P->sectors < 0 || P->sectors > 1)
         return 0;
     if (P->num_shards == 0 || (P->num_shards & (P->num_shards - 1)))
         return 0;
@@ -367,10 +384,10 @@ static int check_offsets(const int64_t *off, int64_t n)
  * caller-zeroed or holding an earlier image.  Returns 0, or -1 on bad
  * arguments. */
 int orc_insert(uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t n,
-               int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+               int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
                int nthreads)
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     if (n == 0)
@@ -383,10 +400,10 @@ int orc_insert(uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t
  * [off[0]>>5, (off[n]+31)>>5); the words are zeroed here and bit g is set iff
  * the k-mer at absolute position g is valid and present. */
 int orc_query(const uint64_t *filter, const uint8_t *seq, const int64_t *off, int64_t n,
-              int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+              int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
               uint32_t *out, int nthreads)
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     if (n == 0)
@@ -400,10 +417,10 @@ int orc_query(const uint64_t *filter, const uint8_t *seq, const int64_t *off, in
 /* The k-mer at absolute position g (one record lookup, then from scratch).
  * Returns 1 if valid (shard and K filled), 0 if not, -1 on bad arguments. */
 int orc_kmer_info(const uint8_t *seq, const int64_t *off, int64_t n, int64_t g,
-                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
                   uint64_t *shard, uint64_t K[4])
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || n <= 0 || g < off[0] || g >= off[n])
         return -1;
     int64_t r = record_of(off, n, g);
@@ -416,10 +433,10 @@ int orc_kmer_info(const uint8_t *seq, const int64_t *off, int64_t n, int64_t g,
  * paper's insert issues one atomicOr per non-zero word per run; *atomics
  * receives that count.  Single-threaded, from scratch per k-mer. */
 int orc_count_runs(const uint8_t *seq, const int64_t *off, int64_t n,
-                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
                    int64_t *valid_kmers, int64_t *runs, int64_t *atomics)
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     int64_t nv = 0, nr = 0, na = 0;
@@ -464,10 +481,10 @@ int orc_count_runs(const uint8_t *seq, const int64_t *off, int64_t n,
  * arguments. */
 int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
                    const int64_t *pos, int64_t count,
-                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+                   int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
                    uint8_t *valid, uint64_t *shard, uint64_t *K)
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || n <= 0)
         return -1;
     for (int64_t i = 0; i < count; i++) {
@@ -487,10 +504,10 @@ int orc_kmer_batch(const uint8_t *seq, const int64_t *off, int64_t n,
  * sparse image.  rows must hold one entry per k-mer position; *count
  * receives the number of valid k-mers written. */
 int orc_kmer_rows(const uint8_t *seq, const int64_t *off, int64_t n,
-                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet,
+                  int k, int m, int s, int H, uint64_t num_shards, uint64_t seed, int alphabet, int sectors,
                   uint64_t *shard, uint64_t *K, int64_t *count)
 {
-    orc_params P = {k, m, s, H, num_shards, seed, alphabet};
+    orc_params P = {k, m, s, H, num_shards, seed, alphabet, sectors};
     if (!valid_params(&P) || !check_offsets(off, n))
         return -1;
     int64_t c = 0;
