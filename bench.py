@@ -381,9 +381,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="measure every configuration and the sweep grid (one JSON line each)")
+    ap.add_argument("--fig4", action="store_true",
+                    help="the paper's Fig. 4 grid: s 16..31 x m 8..31 x H in {4, 8, 12, 16} at k = 31 "
+                         "(one JSON line per point, then the orderings the paper reports)")
+    ap.add_argument("--fig4-h", default="4,8,12,16")
+    ap.add_argument("--fig4-s", default="16-31")
+    ap.add_argument("--fig4-m", default="8-31")
     args = ap.parse_args()
     if args.suite:
         run_suite(args)
+        return
+    if args.fig4:
+        run_fig4(args)
         return
     rank, world, local = dist_info()
 
@@ -729,6 +738,109 @@ def run_suite(args):
         a_ins, a_qry = spec["make"]()
         measure(name, a_ins, a_qry, spec["bits"], p=spec["p"])
         del a_ins, a_qry
+
+
+def _int_range(spec: str):
+    out = []
+    for part in spec.split(","):
+        a, _, b = part.partition("-")
+        out += list(range(int(a), int(b or a) + 1))
+    return out
+
+
+def run_fig4(args):
+    """The paper's parameter study (Sec. V-B, Fig. 4) at k = 31: every (s, m, H)
+    of the grid inserts the 50 Mbp genome-like reference into its own 2^30-bit
+    filter (the paper: C. elegans into 256 MiB, ~21 bits per k-mer here and
+    there), queries its 10^6 reads (timing) and 10^7 uniform 31-mers absent
+    from the reference (FPR).  Every point is timed on the runtime-parameter
+    kernels (one kernel family for the whole heatmap); points with a compiled
+    strip kernel are timed on it too ("strip").  Times are CUDA-event means
+    of two calls after one untimed call."""
+    import torch
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter, build_lib, _native as N
+    build_lib.build()
+    torch.cuda.set_device(0)
+    st = int(torch.cuda.current_stream().cuda_stream)
+    g_ins, g_qry = synth.genome_like()
+    fq = synth.sweep_queries(g_ins)
+    dev = [torch.from_numpy(x).cuda() for x in (g_ins.seq, g_ins.offsets, g_qry.seq, g_qry.offsets, fq.seq,
+                                                  fq.offsets)]
+    di, dio, dq, dqo, df, dfo = dev
+    out = torch.zeros((g_qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
+    fout = torch.zeros((fq.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
+    nk_i, nk_q = kmer_count(g_ins), kmer_count(g_qry)
+    def timed_pair(sbf):
+        t_i = _timed(torch, lambda: N.sbf_insert(sbf.handle, di.data_ptr(), dio.data_ptr(), g_ins.n_records, st),
+                     warmup=1, reps=2)
+        t_q = _timed(torch, lambda: N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(), g_qry.n_records,
+                                                 out.data_ptr(), st), warmup=1, reps=2)
+        return t_i, t_q
+
+    res = {}
+    for H_ in _int_range(args.fig4_h):
+        for s_ in _int_range(args.fig4_s):
+            for m_ in _int_range(args.fig4_m):
+                # every point on the runtime-parameter kernels (one kernel family
+                # for the whole time heatmap); its FPR is the method's, whatever
+                # the kernel
+                sbf = SuperBloomFilter(1 << 30, k=31, m=m_, s=s_, H=H_, seed=SEED, runtime_kernels=True)
+                t_i, t_q = timed_pair(sbf)
+                N.sbf_query(sbf.handle, df.data_ptr(), dfo.data_ptr(), fq.n_records, fout.data_ptr(), st)
+                torch.cuda.synchronize()
+                if sbf.status() != 0:
+                    raise RuntimeError(f"device status error at s={s_} m={m_} H={H_}")
+                fpr = fpr_of(fout.cpu().numpy().view(np.uint32), fq)
+                sbf.close()
+                line = {"fig4": True, "s": s_, "m": m_, "H": H_, "k": 31, "kernel": "runtime",
+                        "insert_kmers_per_s": nk_i / t_i, "query_kmers_per_s": nk_q / t_q,
+                        "insert_ms": 1e3 * t_i, "query_ms": 1e3 * t_q, "fpr": fpr}
+                spec = SuperBloomFilter(1 << 30, k=31, m=m_, s=s_, H=H_, seed=SEED)
+                if spec.specialized:
+                    u_i, u_q = timed_pair(spec)
+                    line["strip"] = {"insert_kmers_per_s": nk_i / u_i, "query_kmers_per_s": nk_q / u_q,
+                                     "insert_ms": 1e3 * u_i, "query_ms": 1e3 * u_q}
+                spec.close()
+                res[(s_, m_, H_)] = line
+                print(json.dumps(line), flush=True)
+    print(json.dumps({"fig4_orderings": fig4_orderings(res)}), flush=True)
+
+
+def fig4_orderings(res) -> dict:
+    """The paper's Sec. V-B statements about Fig. 4, each as (ours, the
+    paper's), where the grid holds the points; FPR ratios are exact results
+    of the method, times those of this GPU's runtime-parameter kernels (one
+    kernel family for every point)."""
+    def get(s_, m_, H_, key):
+        r = res.get((s_, m_, H_))
+        return None if r is None else r[key]
+
+    def ratio(a, b):
+        return None if a is None or b is None or not b else a / b
+    tot = {k: r["insert_ms"] + r["query_ms"] for k, r in res.items()}
+    out = {
+        "fpr H=8 / H=4 at (28,16)": (ratio(get(28, 16, 8, "fpr"), get(28, 16, 4, "fpr")), 2.0),
+        "fpr H=16 / H=4 at (28,16)": (ratio(get(28, 16, 16, "fpr"), get(28, 16, 4, "fpr")), 5.2),
+        "time H=8 / H=4 at (28,16)": (ratio(tot.get((28, 16, 8)), tot.get((28, 16, 4))), 1.076),
+        "time H=16 / H=4 at (28,16)": (ratio(tot.get((28, 16, 16)), tot.get((28, 16, 4))), 1.659),
+        "fpr s=30 / s=28 at (m,H)=(16,4)": (ratio(get(30, 16, 4, "fpr"), get(28, 16, 4, "fpr")), 1.256),
+        "fpr s=31 / s=28 at (m,H)=(16,4)": (ratio(get(31, 16, 4, "fpr"), get(28, 16, 4, "fpr")), 2.29),
+        "fpr s=28 / s=16 at (m,H)=(16,4)": (ratio(get(28, 16, 4, "fpr"), get(16, 16, 4, "fpr")), 1 - 0.374),
+        "time s=28 / s=16 at (m,H)=(16,4)": (ratio(tot.get((28, 16, 4)), tot.get((16, 16, 4))), 1 - 0.291),
+        "fpr m=12 / m=8 at (s,H)=(28,4)": (ratio(get(28, 12, 4, "fpr"), get(28, 8, 4, "fpr")), 1 - 0.917),
+        "fpr m=16 / m=12 at (s,H)=(28,4)": (ratio(get(28, 16, 4, "fpr"), get(28, 12, 4, "fpr")), 1 - 0.908),
+        "fpr m=18 / m=16 at (s,H)=(28,4)": (ratio(get(28, 18, 4, "fpr"), get(28, 16, 4, "fpr")), 1.035),
+        "time m=18 / m=16 at (s,H)=(28,4)": (ratio(tot.get((28, 18, 4)), tot.get((28, 16, 4))), 1.085),
+        "fpr m=31 / m=16 at (s,H)=(28,4)": (ratio(get(28, 31, 4, "fpr"), get(28, 16, 4, "fpr")), 4.8),
+    }
+    # Pareto set (minimise FPR and insert+query time jointly)
+    pts = sorted(res, key=lambda k: (res[k]["fpr"], tot[k]))
+    pareto, best_t = [], float("inf")
+    for k in pts:
+        if tot[k] < best_t:
+            pareto.append(k)
+            best_t = tot[k]
+    return {"ratios (ours, paper)": out, "pareto (s, m, H)": pareto}
 
 
 def run_e2e(torch, N, sbf, ins, qry, nk_total, pg, world, steps):

@@ -101,6 +101,29 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
  * Returns NULL on error, like sbf_create. */
 sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet);
 
+/* Creation flags of sbf_create_ex. */
+#define SBF_FLAG_HASHED_SECTORS 1  /* hash-chosen sectors for H < 4 (see sbf_create_ex) */
+#define SBF_FLAG_RUNTIME_KERNELS 2 /* always the runtime-parameter kernels (see sbf_create_ex) */
+
+/* sbf_create_alphabet with creation flags (sbf_create_alphabet is this call
+ * with flags = 0).  SBF_FLAG_HASHED_SECTORS is an extension of the paper's
+ * layout (Sec. IV-B, Algorithm 2: hash i of an s-mer sets a bit in word
+ * i mod 4 of the shard), which leaves words H..3 of every shard empty when
+ * H < 4.  With the flag and H < 4, hash i sets its bit in the word given by
+ * the two bits of its slice just above its six position bits:
+ * (hs >> (i * floor(64/H) + 6)) & 3 (slices are >= 21 bits wide there), so a
+ * k-mer's bits spread over all 256 bits of its shard; the position is
+ * unchanged.  For H >= 4 the flag has no effect.  SBF_FLAG_RUNTIME_KERNELS
+ * runs every call on the runtime-parameter kernels even where a compile-time
+ * specialisation of (k, m, s, H) exists (same results, slower; for comparing
+ * parameter points on one kernel family, or the two families on one point);
+ * sbf_is_specialized then returns 0.  Any other flag bit is
+ * SBF_ERR_INVALID_ARG.  Returns NULL on error, like sbf_create. */
+sbf_filter *sbf_create_ex(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet, int flags);
+
+/* The creation flags of f (SBF_FLAG_*), or -1 for NULL. */
+int sbf_get_flags(const sbf_filter *f);
+
 /* The filter's alphabet (SBF_ALPHABET_*), or -1 for NULL. */
 int sbf_get_alphabet(const sbf_filter *f);
 

@@ -23,6 +23,8 @@ _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "sbf_create": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64]),
     "sbf_create_alphabet": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64, _i32]),
+    "sbf_create_ex": (_vp, [_u64, _i32, _i32, _i32, _i32, _u64, _i32, _i32]),
+    "sbf_get_flags": (_i32, [_vp]),
     "sbf_query_dense": (_i32, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "sbf_get_alphabet": (_i32, [_vp]),
     "sbf_destroy": (None, [_vp]),
@@ -177,6 +179,22 @@ def sbf_create_alphabet(num_bits: int, k: int, m: int, s: int, H: int, seed: int
     if not h:
         raise SBFError(SBF_ERR_INVALID_ARG, "sbf_create_alphabet", last_error())
     return h
+
+
+# creation flags (SBF_FLAG_* of sbf.h)
+FLAG_HASHED_SECTORS = 1
+FLAG_RUNTIME_KERNELS = 2
+
+
+def sbf_create_ex(num_bits: int, k: int, m: int, s: int, H: int, seed: int, alphabet, flags: int) -> int:
+    h = load().sbf_create_ex(num_bits, k, m, s, H, seed & (2**64 - 1), alphabet_id(alphabet), flags)
+    if not h:
+        raise SBFError(SBF_ERR_INVALID_ARG, "sbf_create_ex", last_error())
+    return h
+
+
+def sbf_get_flags(f: int) -> int:
+    return int(load().sbf_get_flags(f))
 
 
 def sbf_query_dense(f: int, seq: int, n_records: int, record_len: int, out_bits: int, stream: int = 0) -> None:

@@ -109,9 +109,10 @@ __device__ __forceinline__ int64_t start_at_or_below(const uint32_t *bm, int j, 
     return b ? t0 + 32 * w + 31 - __clz(b) : prev;
 }
 
-// The s-mer's H bits as four word masks; compile-time H when H_ > 0.
+// The s-mer's H bits as four word masks; compile-time H when H_ > 0
+// (`sectors`: hash-chosen words for H < 4, sector_word).
 template <int H_>
-__device__ __forceinline__ void smer_words(uint64_t hs, int H, uint64_t K[4]) {
+__device__ __forceinline__ void smer_words(uint64_t hs, int H, uint64_t K[4], int sectors) {
     K[0] = K[1] = K[2] = K[3] = 0ull;
     if constexpr (H_ > 0) {
         constexpr int SW = 64 / H_;
@@ -120,10 +121,13 @@ __device__ __forceinline__ void smer_words(uint64_t hs, int H, uint64_t K[4]) {
             uint32_t pos;
             if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
             else pos = (uint32_t)((hs * salt_of(i)) >> 58);
-            K[i & 3] |= 1ull << pos;
+            if (H_ < 4 && sectors)
+                or_into_word(K, sector_word(hs, i, SW), 1ull << pos);
+            else
+                K[i & 3] |= 1ull << pos;
         }
     } else {
-        smer_bits_runtime(hs, H, K);
+        smer_bits_runtime(hs, H, K, sectors);
     }
 }
 
@@ -142,7 +146,9 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
     const int w = k - m + 1, z1 = k - s + 1, L = m > s ? m : s;
     const int kspan = B * k;
     const uint64_t seed_m = a.seed, seed_s = ~a.seed;
-    const int n_words = kStatic ? (H_ < 4 ? H_ : 4) : (a.H < 4 ? a.H : 4);
+    // words a k-mer's bits can reach: 0..H-1 when H < 4 (word i mod 4), all
+    // four with hash-chosen sectors or H >= 4
+    const int n_words = a.sectors ? 4 : kStatic ? (H_ < 4 ? H_ : 4) : (a.H < 4 ? a.H : 4);
     const int64_t base = lo & ~int64_t(31);
     const int64_t n_tiles = (hi - base + TB - 1) / TB;
     // this block's contiguous tile range
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kAlphaThreads) alphabet_kernel(LaunchArgs a) {
                 for (int i = 0; i < L; ++i) v = (v << BITS) | (sm.code[pos + B * i] & ((1u << BITS) - 1u));
                 sm.hm[u] = hash_minimizer(v >> (BITS * (L - m)), seed_m);
                 uint64_t K[4];
-                smer_words<H_>(hash_smer(v >> (BITS * (L - s)), seed_s), a.H, K);
+                smer_words<H_>(hash_smer(v >> (BITS * (L - s)), seed_s), a.H, K, a.sectors);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) sm.sk[q][u] = K[q];
             };
@@ -378,7 +384,7 @@ constexpr AlphaEntry alpha_entry() {
 }  // namespace
 
 bool find_alphabet_kernels(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
-                           bool *specialized) {
+                           bool *specialized, bool may_specialise) {
     // the benchmarked points (protein 12/8/10/4, triplet 10/5/8/4), then the
     // runtime-parameter kernels
     static const AlphaEntry table[] = {
@@ -386,7 +392,7 @@ bool find_alphabet_kernels(int alphabet, int k, int m, int s, int H, const void 
         alpha_entry<kAlphabetTriplet, 10, 5, 8, 4>(),
     };
     for (const AlphaEntry &e : table)
-        if (e.alphabet == alphabet && e.k == k && e.m == m && e.s == s && e.H == H) {
+        if (may_specialise && e.alphabet == alphabet && e.k == k && e.m == m && e.s == s && e.H == H) {
             *insert = e.insert;
             *query = e.query;
             *specialized = true;

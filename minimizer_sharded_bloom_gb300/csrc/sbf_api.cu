@@ -148,6 +148,7 @@ sbf::LaunchArgs make_args(const sbf_filter *f, const char *seq, const int64_t *o
     la.rec_len = 0;
     la.nonuniform = nullptr;
     la.out_words_end = INT64_MAX;
+    la.sectors = f->sectors;
     la.wait_test = 0;
     return la;
 }
@@ -240,7 +241,20 @@ sbf_filter *sbf_create(uint64_t num_bits, int k, int m, int s, int H, uint64_t s
 }
 
 sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet) {
+    return sbf_create_ex(num_bits, k, m, s, H, seed, alphabet, 0);
+}
+
+int sbf_get_flags(const sbf_filter *f) {
+    if (!f) return -1;
+    return (f->sectors ? SBF_FLAG_HASHED_SECTORS : 0) | (f->runtime_only ? SBF_FLAG_RUNTIME_KERNELS : 0);
+}
+
+sbf_filter *sbf_create_ex(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet, int flags) {
     g_last_error.clear();
+    if (flags & ~(SBF_FLAG_HASHED_SECTORS | SBF_FLAG_RUNTIME_KERNELS)) {
+        fail(SBF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+        return nullptr;
+    }
     if (num_bits < 1) {
         fail(SBF_ERR_INVALID_ARG, "num_bits must be >= 1");
         return nullptr;
@@ -273,6 +287,9 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     f->H = H;
     f->alphabet = alphabet;
     f->seed = seed;
+    f->sectors = (flags & SBF_FLAG_HASHED_SECTORS) ? 1 : 0;
+    f->runtime_only = (flags & SBF_FLAG_RUNTIME_KERNELS) != 0;
+    const bool may_specialise = !f->runtime_only;
     f->num_shards = shards;
     cudaError_t e = cudaGetDevice(&f->device);
     int sms = 0;
@@ -303,17 +320,17 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     int threads = 0;
     // The strip kernels key runs by shard with bit 31 marking invalid k-mers.
     int threads_query = 0;
-    if (alphabet != SBF_ALPHABET_DNA && shards <= (1ull << 31) &&
+    if (alphabet != SBF_ALPHABET_DNA && may_specialise && shards <= (1ull << 31) &&
         sbf::find_alphabet_strip(alphabet, k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
         f->strip = true;
         threads_query = threads;
     } else if (alphabet != SBF_ALPHABET_DNA) {
         bool spec = false;
-        sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec);
+        sbf::find_alphabet_kernels(alphabet, k, m, s, H, &ins, &qry, &spec, may_specialise);
         f->specialized = spec;
         threads = 256;
-    } else if (shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
+    } else if (may_specialise && shards <= (1ull << 31) && sbf::find_specialized(k, m, s, H, &ins, &qry, &threads)) {
         f->specialized = true;
         f->strip = true;
     } else {
@@ -328,7 +345,7 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
     f->threads_query = threads_query;
     f->grid_insert = grid_for(ins, threads, sms);
     f->grid_query = grid_for(qry, threads_query, sms);
-    if (alphabet == SBF_ALPHABET_DNA && shards <= (1ull << 31)) {
+    if (alphabet == SBF_ALPHABET_DNA && may_specialise && shards <= (1ull << 31)) {
         f->dense_query_kernel = sbf::dense_query_kernel(k, m, s, H, &f->threads_dense);
         if (f->dense_query_kernel) {
             f->grid_dense = grid_for(f->dense_query_kernel, f->threads_dense, sms);

@@ -36,6 +36,7 @@ struct LaunchArgs {
                               // offsets check saw records of different lengths (else nullptr)
     int64_t out_words_end;    // query: answer words at or past this index are not written
                               // (a chunk of a larger batch cut inside a record); else INT64_MAX
+    int sectors;              // 1: hash-chosen sectors for H < 4 (sector_word); 0: word i mod 4
     int wait_test;            // failure-detection test: > 0 = before any work, one thread waits
                               // on an mbarrier that nothing completes, giving up after
                               // wait_test polls; the kernel then reports the timeout and
@@ -92,13 +93,33 @@ __constant__ const uint64_t kSalt[kMaxH] = {
     salt_of(16), salt_of(17), salt_of(18), salt_of(19), salt_of(20), salt_of(21), salt_of(22), salt_of(23),
     salt_of(24), salt_of(25), salt_of(26), salt_of(27), salt_of(28), salt_of(29), salt_of(30), salt_of(31)};
 
+// The word of hash i with hash-chosen sectors (filters created with
+// SBF_FLAG_HASHED_SECTORS, H < 4 only): the two bits of slice i (width W =
+// floor(64/H) >= 21) just above its six position bits.  The paper's layout
+// (Sec. IV-B) uses word i mod 4, which leaves words H..3 empty when H < 4.
+__device__ __forceinline__ uint32_t sector_word(uint64_t hs, int i, int W) {
+    return (uint32_t)(hs >> (i * W + 6)) & 3u;
+}
+
+// x into the word K[w] of a runtime w, without indexing K dynamically (K
+// stays in registers).
+__device__ __forceinline__ void or_into_word(uint64_t K[4], uint32_t w, uint64_t x) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) K[q] |= w == (uint32_t)q ? x : 0ull;
+}
+
 // OR the H bits of one s-mer hash into four word masks (Sec. IV-B: hash i ->
-// word i mod 4).  Sec. IV-G: bit-slicing with slice width floor(64/H) while it
-// is at least 6 bits; beyond, the top 6 bits of hs * salt(i).
+// word i mod 4; with `sectors` and H < 4, sector_word).  Sec. IV-G:
+// bit-slicing with slice width floor(64/H) while it is at least 6 bits;
+// beyond, the top 6 bits of hs * salt(i).
 // (Loops unrolled to their bounds so that K stays in registers.)
-__device__ __forceinline__ void smer_bits_runtime(uint64_t hs, int H, uint64_t K[4]) {
+__device__ __forceinline__ void smer_bits_runtime(uint64_t hs, int H, uint64_t K[4], int sectors = 0) {
     const int W = 64 / H;
-    if (W >= 6) {
+    if (sectors && H < 4) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (i < H) or_into_word(K, sector_word(hs, i, W), 1ull << ((hs >> (i * W)) & 63u));
+    } else if (W >= 6) {
 #pragma unroll
         for (int i = 0; i < 10; ++i)
             if (i < H) K[i & 3] |= 1ull << ((hs >> (i * W)) & 63u);

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256) generic_kernel(LaunchArgs a) {
                     shard = mu & a.shard_mask;
                     for (int j = 0; j <= a.k - a.s; ++j) {
                         const uint64_t y = (kv >> (2 * (a.k - a.s - j))) & mask_s;
-                        smer_bits_runtime(hash_smer(y, seed_s), a.H, K);
+                        smer_bits_runtime(hash_smer(y, seed_s), a.H, K, a.sectors);
                     }
                     valid = true;
                 }

@@ -12,6 +12,7 @@ struct sbf_filter {
     int k = 0, m = 0, s = 0, H = 0;
     int alphabet = SBF_ALPHABET_DNA;
     uint64_t seed = 0;
+    int sectors = 0;            // 1: hash-chosen sectors for H < 4 (SBF_FLAG_HASHED_SECTORS)
     uint64_t num_shards = 0;
     uint64_t *words = nullptr;  // num_shards * 4 words
     int *status = nullptr;      // sticky device status
@@ -26,6 +27,7 @@ struct sbf_filter {
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
     bool specialized = false;
+    bool runtime_only = false;  // SBF_FLAG_RUNTIME_KERNELS: never a compile-time specialisation
     bool strip = false;         // insert/query kernels are strip kernels (bounded mbarrier waits)
     void *stager = nullptr;     // host-facing staging buffers, created on first use
     int64_t host_chunk = int64_t(1) << 26;  // host-facing chunk, in positions

@@ -29,7 +29,7 @@ bool find_alphabet_strip(int alphabet, int k, int m, int s, int H, const void **
 // else the runtime-parameter kernel.  False for any other alphabet.  256
 // threads per block.
 bool find_alphabet_kernels(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,
-                           bool *specialized);
+                           bool *specialized, bool may_specialise = true);
 
 // Compile-time specialised kernels.  Returns false when (k, m, s, H) has no
 // specialisation; *insert / *query / *threads are set otherwise.

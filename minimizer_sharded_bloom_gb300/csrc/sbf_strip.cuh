@@ -59,15 +59,23 @@ namespace sbf {
 // word values are first copied into registers of their own, so that the
 // accumulator can be reset at once instead of waiting until the reductions
 // have read their operands.
+// Words a run can touch: H < 4 fills words 0..H-1 (hash i in word i mod 4),
+// or any word with hash-chosen sectors; H >= 4 all four.
 template <int H>
-__device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
+__device__ __forceinline__ bool word_used(int wd, int sectors) {
+    return wd < H || (H < 4 && sectors);
+}
+
+template <int H>
+__device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8], int sectors) {
     uint64_t v[4];
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd)
         asm volatile("mov.b64 %0, {%1, %2};" : "=l"(v[wd]) : "r"(acc[2 * wd]), "r"(acc[2 * wd + 1]));
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
-        if (wd >= H) continue;
+        if (!word_used<H>(wd, sectors)) continue;
+        if (H < 4 && sectors && !v[wd]) continue;
         asm volatile("red.global.or.b64 [%0], %1;" ::"l"(F + wd), "l"(v[wd]) : "memory");
     }
 }
@@ -81,7 +89,7 @@ __device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
 // ceil(4 * runs / n_active) <= 128, is the same on every lane.
 template <int H>
 __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const uint32_t acc[8], bool flush,
-                                           unsigned am) {
+                                           unsigned am, int sectors) {
     const unsigned fm = __ballot_sync(am, flush);
     if (!fm) return;
     const int lane = threadIdx.x & 31;
@@ -106,7 +114,7 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
                 hi = h;
             }
         }
-        if (pidx < pairs && wd < H && (lo | hi)) {
+        if (pidx < pairs && word_used<H>(wd, sectors) && (lo | hi)) {
             const uint64_t v = ((uint64_t)hi << 32) | lo;
             asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)k * 4 + wd), "l"(v) : "memory");
         }
@@ -124,7 +132,7 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
 template <int H, int QN>
 __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int &head, int &tail, bool flush,
                                            uint32_t key, const uint32_t acc[8], int lane, int drain_at,
-                                           uint64_t *words) {
+                                           uint64_t *words, int sectors) {
     const unsigned fm = __ballot_sync(0xffffffffu, flush);
     if (fm) {
         if (flush) {
@@ -144,7 +152,7 @@ __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int
                 const int e = (head + (lane >> 2)) & (QN - 1);
                 const uint2 v = reinterpret_cast<const uint2 *>(q_acc + 8 * e)[wd];
                 const uint64_t x = ((uint64_t)v.y << 32) | v.x;
-                if (wd < H && x)
+                if (word_used<H>(wd, sectors) && x)
                     asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)q_key[e] * 4 + wd), "l"(x)
                                  : "memory");
             }
@@ -385,13 +393,14 @@ struct StripSmem {
 };
 
 
-// The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1).
+// The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1);
+// `sectors` (hash-chosen words, H < 4) is the launch's flag.
 // kTable: the one-hot halves of a bit position come from a 64-entry shared
 // table (tab[p] = halves of 1 << p), one shared load instead of a variable
 // 64-bit shift on the ALU pipe (the query, ALU-bound, gains ~4 %; the insert
 // does not).
 template <int H, bool kTable>
-__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab) {
+__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab, int sectors) {
     constexpr int SW = 64 / H;
 #pragma unroll
     for (int j = 0; j < 8; ++j) m[j] = 0u;
@@ -400,6 +409,17 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const ui
         uint32_t pos;
         if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
         else pos = (uint32_t)((hs * salt_of(i)) >> 58);
+        if (H < 4 && sectors) {
+            // hash-chosen sector (H < 4): the word is sector_word, not i mod 4
+            const uint32_t w = sector_word(hs, i, SW);
+            const uint64_t one = 1ull << pos;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                m[2 * q] |= w == (uint32_t)q ? (uint32_t)one : 0u;
+                m[2 * q + 1] |= w == (uint32_t)q ? (uint32_t)(one >> 32) : 0u;
+            }
+            continue;
+        }
         if constexpr (kTable) {
             const uint2 one = tab[pos];
             m[2 * (i & 3)] |= one.x;
@@ -759,14 +779,14 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                     codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
                     for (int z = 0; z < Z; ++z)
-                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
+                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot, a.sectors);
                 } else {
 #pragma unroll
                     for (int i = 0; i < S - 1; ++i) vb = (vb << BITS) | sm.pcode[kk0 + 16 + i];
 #pragma unroll
                     for (int z = 0; z < Z; ++z) {
                         vb = (vb << BITS) | sm.pcode[kk0 + 16 + z + S - 1];
-                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot);
+                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot, a.sectors);
                     }
 #pragma unroll
                     for (int i = 0; i < M - 1; ++i) va = (va << BITS) | sm.pcode[kk0 + 15 + i];
@@ -874,7 +894,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             vb = (vb << BITS) | sm.pcode[kb + 16 + Z + i + S - 1];
                             sv = vb & kMaskS;
                         }
-                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot);
+                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot, a.sectors);
                         // OR of the k-mer's older s-mers (its newest is mk[Z])
                         uint32_t older[8];
 #pragma unroll
@@ -892,11 +912,11 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                                 const bool fl = key != cur_key && !(cur_key >> 31);
                                 if (am == 0xffffffffu)
                                     queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head,
-                                                      q_tail, fl, cur_key, acc, tid & 31, 8, words);
+                                                      q_tail, fl, cur_key, acc, tid & 31, 8, words, a.sectors);
                                 else if (fl)
-                                    flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                                    flush_run<H>(words + (uint64_t)cur_key * 4, acc, a.sectors);
                             } else {
-                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am);
+                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am, a.sectors);
                             }
                             const uint32_t same = key == cur_key ? 1u : 0u;
 #pragma unroll
@@ -946,11 +966,11 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                     // the strip's last runs, then everything still queued
                     if (am == 0xffffffffu)
                         queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head, q_tail,
-                                          !(cur_key >> 31), cur_key, acc, tid & 31, 1, words);
+                                          !(cur_key >> 31), cur_key, acc, tid & 31, 1, words, a.sectors);
                     else if (!(cur_key >> 31))
-                        flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                        flush_run<H>(words + (uint64_t)cur_key * 4, acc, a.sectors);
                 } else {
-                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am);
+                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am, a.sectors);
                 }
             }
         }

@@ -31,11 +31,20 @@ class SuperBloomFilter:
     """An SBF on the current CUDA device (sbf_create / sbf_destroy)."""
 
     def __init__(self, num_bits: int, k: int = 31, m: int = 16, s: int = 28, H: int = 4,
-                 seed: int = 0, alphabet="dna"):
+                 seed: int = 0, alphabet="dna", sectors: str = "fixed", runtime_kernels: bool = False):
         """alphabet: "dna" (default), "protein" or "dna_triplet" (Sec. IV-A;
-        k <= 32, 12, 10 respectively), or the SBF_ALPHABET_* value."""
+        k <= 32, 12, 10 respectively), or the SBF_ALPHABET_* value.
+        sectors: "fixed" (the paper's layout, hash i in word i mod 4) or
+        "hashed" (hash-chosen words for H < 4; SBF_FLAG_HASHED_SECTORS).
+        runtime_kernels: always the runtime-parameter kernels
+        (SBF_FLAG_RUNTIME_KERNELS)."""
+        if sectors not in ("fixed", "hashed"):
+            raise ValueError(f"sectors must be 'fixed' or 'hashed', not {sectors!r}")
         self.alphabet = N.alphabet_id(alphabet)
-        self._h = N.sbf_create_alphabet(int(num_bits), k, m, s, H, seed, self.alphabet)
+        self.sectors = sectors
+        flags = (N.FLAG_HASHED_SECTORS if sectors == "hashed" else 0) | \
+            (N.FLAG_RUNTIME_KERNELS if runtime_kernels else 0)
+        self._h = N.sbf_create_ex(int(num_bits), k, m, s, H, seed, self.alphabet, flags)
         self.k, self.m, self.s, self.H = k, m, s, H
         self.seed = seed & (2**64 - 1)
         self.num_shards = N.sbf_num_shards(self._h)

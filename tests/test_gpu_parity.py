@@ -462,3 +462,27 @@ def test_host_entry_points(torch, pinned, params, mode):
     assert_images_equal(sbf.to_numpy(), F)
     sbf.query_host(s_q, o_q, out=out)
     assert_words_equal(out, oracle_answers(F, qry.seq, qry.offsets, params, 21), qry.offsets)
+
+
+@pytest.mark.parametrize("params", [dict(k=31, m=16, s=28, H=4), dict(k=31, m=12, s=20, H=8),
+                                    dict(k=31, m=21, s=31, H=1), dict(k=31, m=16, s=28, H=16)])
+def test_runtime_kernels_flag_matches_strip_kernels(params):
+    """SBF_FLAG_RUNTIME_KERNELS runs a specialised point on the runtime-
+    parameter kernels: the images and answers equal the strip kernels'."""
+    torch = need_gpu()
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter
+    rng = np.random.default_rng(sum(params.values()))
+    ins = synth.random_records(rng, 10, 200, 40_000, n_prob=0.001, lower_prob=0.01)
+    qry = synth.random_records(rng, 400, 20, 300, n_prob=0.002)
+    qseq = np.concatenate([ins.seq, qry.seq])
+    qoff = np.concatenate([ins.offsets, ins.offsets[-1] + qry.offsets[1:]])
+    res = []
+    for rt in (False, True):
+        sbf = SuperBloomFilter(1 << 22, seed=9, runtime_kernels=rt, **params)
+        assert sbf.specialized == (not rt)
+        gpu_insert(torch, sbf, ins.seq, ins.offsets)
+        res.append((sbf.to_numpy(), gpu_query(torch, sbf, qseq, qoff)))
+        assert sbf.status() == 0
+        sbf.close()
+    assert_images_equal(res[1][0], res[0][0])
+    assert_words_equal(res[1][1], res[0][1], qoff)
