@@ -666,12 +666,12 @@ def run_suite(args):
     def dev(wl):
         return torch.from_numpy(wl.seq).cuda(), torch.from_numpy(wl.offsets).cuda()
 
-    def measure(name, ins, qry, bits, k=K, m=M, s=S, H=H, fpr_qry=None, extra=None, p=None):
+    def measure(name, ins, qry, bits, k=K, m=M, s=S, H=H, fpr_qry=None, extra=None, p=None, sectors="fixed"):
         alphabet = "dna"
         if p is not None:
             k, m, s, H, alphabet = p["k"], p["m"], p["s"], p["H"], p["alphabet"]
         B = 3 if alphabet == "dna_triplet" else 1
-        sbf = SuperBloomFilter(bits, k=k, m=m, s=s, H=H, seed=SEED, alphabet=alphabet)
+        sbf = SuperBloomFilter(bits, k=k, m=m, s=s, H=H, seed=SEED, alphabet=alphabet, sectors=sectors)
         di, dio = dev(ins)
         dq, dqo = dev(qry)
         out = torch.zeros((qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
@@ -705,7 +705,7 @@ def run_suite(args):
             del ones
         else:
             fpr, n_fpr = fpr_of(words, fq, k, B), fpr_count(fq, k, B)
-        line = {"suite": name, "alphabet": alphabet, "k": k, "m": m, "s": s, "H": H,
+        line = {"suite": name, "alphabet": alphabet, "k": k, "m": m, "s": s, "H": H, "sectors": sectors,
                 "filter_bits": bits, "specialized": sbf.specialized,
                 "insert_kmers": kmer_count(ins, k, B), "query_kmers": kmer_count(qry, k, B),
                 "insert_kmers_per_s": kmer_count(ins, k, B) / t_ins,
@@ -728,6 +728,12 @@ def run_suite(args):
     for H_ in (12, 16):  # the paper's larger hash counts (salted multiply, Sec. IV-G)
         measure("sweep", g_ins, g_qry, 1 << 30, m=16, s=28, H=H_, fpr_qry=sweep_q,
                 extra={"fpr_queries": "10,000,000 uniform 31-mers absent from the inserted set"})
+    # hash-chosen sectors (SBF_FLAG_HASHED_SECTORS) against the paper's layout
+    # where it applies (H < 4)
+    for s_ in (20, 24, 28, 31):
+        for H_ in (1, 2):
+            measure("sweep", g_ins, g_qry, 1 << 30, m=16, s=s_, H=H_, fpr_qry=sweep_q, sectors="hashed",
+                    extra={"fpr_queries": "10,000,000 uniform 31-mers absent from the inserted set"})
     del g_ins, g_qry, sweep_q
     i_ins, i_qry = synth.irregular()
     i_qry.meta["is_random"] = np.ones(i_qry.n_records, dtype=bool)

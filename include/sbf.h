@@ -113,7 +113,9 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
  * the two bits of its slice just above its six position bits:
  * (hs >> (i * floor(64/H) + 6)) & 3 (slices are >= 21 bits wide there), so a
  * k-mer's bits spread over all 256 bits of its shard; the position is
- * unchanged.  For H >= 4 the flag has no effect.  SBF_FLAG_RUNTIME_KERNELS
+ * unchanged.  Such a filter runs on the runtime-parameter kernels (the
+ * compile-time specialisations keep the paper's layout), so
+ * sbf_is_specialized returns 0.  For H >= 4 the flag has no effect.  SBF_FLAG_RUNTIME_KERNELS
  * runs every call on the runtime-parameter kernels even where a compile-time
  * specialisation of (k, m, s, H) exists (same results, slower; for comparing
  * parameter points on one kernel family, or the two families on one point);

@@ -246,7 +246,7 @@ sbf_filter *sbf_create_alphabet(uint64_t num_bits, int k, int m, int s, int H, u
 
 int sbf_get_flags(const sbf_filter *f) {
     if (!f) return -1;
-    return (f->sectors ? SBF_FLAG_HASHED_SECTORS : 0) | (f->runtime_only ? SBF_FLAG_RUNTIME_KERNELS : 0);
+    return (f->sectors ? SBF_FLAG_HASHED_SECTORS : 0) | (f->runtime_requested ? SBF_FLAG_RUNTIME_KERNELS : 0);
 }
 
 sbf_filter *sbf_create_ex(uint64_t num_bits, int k, int m, int s, int H, uint64_t seed, int alphabet, int flags) {
@@ -288,7 +288,10 @@ sbf_filter *sbf_create_ex(uint64_t num_bits, int k, int m, int s, int H, uint64_
     f->alphabet = alphabet;
     f->seed = seed;
     f->sectors = (flags & SBF_FLAG_HASHED_SECTORS) ? 1 : 0;
-    f->runtime_only = (flags & SBF_FLAG_RUNTIME_KERNELS) != 0;
+    // hash-chosen sectors (H < 4) run on the runtime-parameter kernels: the
+    // compile-time specialisations keep the paper's layout only
+    f->runtime_requested = (flags & SBF_FLAG_RUNTIME_KERNELS) != 0;
+    f->runtime_only = f->runtime_requested || (f->sectors && H < 4);
     const bool may_specialise = !f->runtime_only;
     f->num_shards = shards;
     cudaError_t e = cudaGetDevice(&f->device);
@@ -339,6 +342,16 @@ sbf_filter *sbf_create_ex(uint64_t num_bits, int k, int m, int s, int H, uint64_
         threads = 256;
     }
     if (threads_query == 0) threads_query = threads;
+    // a DNA filter several times larger than L2: every run's shard update is a
+    // DRAM read-modify-write, and the insert flushes runs through its warp's
+    // run queue (one 32-byte request per run) where it has that form
+    if (alphabet == SBF_ALPHABET_DNA && f->strip) {
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, f->device) == cudaSuccess && l2 > 0 &&
+            shards * 32 > (uint64_t)sbf::kQueuedInsertL2Multiple * (uint64_t)l2)
+            if (const void *q = sbf::queued_insert_kernel(k, m, s, H)) ins = q;
+        cudaGetLastError();
+    }
     f->insert_kernel = ins;
     f->query_kernel = qry;
     f->threads = threads;

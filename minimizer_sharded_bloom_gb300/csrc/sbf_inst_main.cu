@@ -3,7 +3,8 @@
 // query kernel is the dense-capable one (records of at most kDenseMax bytes,
 // one per strip): sbf_query_dense calls it with a record length, and the CSR
 // query calls it too, where it takes the dense geometry for a batch whose
-// records the offsets check found to be all of one length.
+// records the offsets check found to be all of one length.  Its insert also
+// comes with the run-queue flush (FQ = 1) for filters much larger than L2.
 #include "sbf_kernels.h"
 #include "sbf_registry.h"
 
@@ -18,6 +19,12 @@ const StripEntry kStripEntriesMain[] = {
                reinterpret_cast<const void *>(&strip_kernel<31, 16, 28, 4, true, 0, kDenseMax>),
                MainDense::NT}};
 const int kStripCountMain = 1;
+
+const void *queued_insert_kernel(int k, int m, int s, int H) {
+    if (k == 31 && m == 16 && s == 28 && H == 4)
+        return reinterpret_cast<const void *>(&strip_kernel<31, 16, 28, 4, false, 0, 0, 1>);
+    return nullptr;
+}
 
 const void *dense_query_kernel(int k, int m, int s, int H, int *threads) {
     if (k == 31 && m == 16 && s == 28 && H == 4) {

@@ -27,7 +27,8 @@ struct sbf_filter {
     int grid_insert = 0, grid_query = 0;
     int grid_check = 0;
     bool specialized = false;
-    bool runtime_only = false;  // SBF_FLAG_RUNTIME_KERNELS: never a compile-time specialisation
+    bool runtime_only = false;  // never a compile-time specialisation (the flag, or hashed sectors)
+    bool runtime_requested = false;  // SBF_FLAG_RUNTIME_KERNELS given at creation
     bool strip = false;         // insert/query kernels are strip kernels (bounded mbarrier waits)
     void *stager = nullptr;     // host-facing staging buffers, created on first use
     int64_t host_chunk = int64_t(1) << 26;  // host-facing chunk, in positions

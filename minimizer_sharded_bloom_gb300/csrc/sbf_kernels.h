@@ -19,6 +19,12 @@ __global__ void check_offsets_kernel(const int64_t *off, int64_t n, int *status,
 constexpr int kDenseMax = 160;
 const void *dense_query_kernel(int k, int m, int s, int H, int *threads);
 
+// The insert strip kernel with the warp run-queue flush (FQ = 1) at (k, m,
+// s, H), or nullptr; the same block size as the filter's insert kernel.
+const void *queued_insert_kernel(int k, int m, int s, int H);
+// Filters of more than this many L2 sizes take the queued insert.
+constexpr int kQueuedInsertL2Multiple = 8;
+
 // The protein and triplet alphabets' strip-kernel specialisations (shards
 // <= 2^31): false when (alphabet, k, m, s, H) has none.
 bool find_alphabet_strip(int alphabet, int k, int m, int s, int H, const void **insert, const void **query,

@@ -59,23 +59,15 @@ namespace sbf {
 // word values are first copied into registers of their own, so that the
 // accumulator can be reset at once instead of waiting until the reductions
 // have read their operands.
-// Words a run can touch: H < 4 fills words 0..H-1 (hash i in word i mod 4),
-// or any word with hash-chosen sectors; H >= 4 all four.
 template <int H>
-__device__ __forceinline__ bool word_used(int wd, int sectors) {
-    return wd < H || (H < 4 && sectors);
-}
-
-template <int H>
-__device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8], int sectors) {
+__device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
     uint64_t v[4];
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd)
         asm volatile("mov.b64 %0, {%1, %2};" : "=l"(v[wd]) : "r"(acc[2 * wd]), "r"(acc[2 * wd + 1]));
 #pragma unroll
     for (int wd = 0; wd < 4; ++wd) {
-        if (!word_used<H>(wd, sectors)) continue;
-        if (H < 4 && sectors && !v[wd]) continue;
+        if (wd >= H) continue;
         asm volatile("red.global.or.b64 [%0], %1;" ::"l"(F + wd), "l"(v[wd]) : "memory");
     }
 }
@@ -89,7 +81,7 @@ __device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8], in
 // ceil(4 * runs / n_active) <= 128, is the same on every lane.
 template <int H>
 __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const uint32_t acc[8], bool flush,
-                                           unsigned am, int sectors) {
+                                           unsigned am) {
     const unsigned fm = __ballot_sync(am, flush);
     if (!fm) return;
     const int lane = threadIdx.x & 31;
@@ -114,7 +106,7 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
                 hi = h;
             }
         }
-        if (pidx < pairs && word_used<H>(wd, sectors) && (lo | hi)) {
+        if (pidx < pairs && wd < H && (lo | hi)) {
             const uint64_t v = ((uint64_t)hi << 32) | lo;
             asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)k * 4 + wd), "l"(v) : "memory");
         }
@@ -132,7 +124,7 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
 template <int H, int QN>
 __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int &head, int &tail, bool flush,
                                            uint32_t key, const uint32_t acc[8], int lane, int drain_at,
-                                           uint64_t *words, int sectors) {
+                                           uint64_t *words) {
     const unsigned fm = __ballot_sync(0xffffffffu, flush);
     if (fm) {
         if (flush) {
@@ -152,7 +144,7 @@ __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int
                 const int e = (head + (lane >> 2)) & (QN - 1);
                 const uint2 v = reinterpret_cast<const uint2 *>(q_acc + 8 * e)[wd];
                 const uint64_t x = ((uint64_t)v.y << 32) | v.x;
-                if (word_used<H>(wd, sectors) && x)
+                if (wd < H && x)
                     asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)q_key[e] * 4 + wd), "l"(x)
                                  : "memory");
             }
@@ -351,7 +343,9 @@ struct StripCfg {
     static constexpr int CODE_WORDS = (TILE + K + 96) / 16 + 4;  // 16 bases per word
     static constexpr int BIT_WORDS = (CODE_WORDS + 1) / 2 + 2;   // one bit per code index
     static constexpr int SW = 64 / H;                   // bit-slice width (Sec. IV-G)
-    static constexpr int SLOTS = A == 0 && D == 0 ? 6 : 4;  // query: staged shards per thread per block
+    // query: staged shards per thread per block (triplets: two, so that four
+    // query CTAs fit an SM)
+    static constexpr int SLOTS = A == 0 && D == 0 ? 6 : A == 2 ? 2 : 4;
     // Triplets (A = 2): a tile covers BYTE_TILE = 3 * TILE bytes in three frame
     // passes; symbol c of pass f is the codon at byte T0 - OFF + f + 3c.
     static constexpr int BYTE_TILE = A == 2 ? 3 * TILE : TILE;
@@ -393,14 +387,15 @@ struct StripSmem {
 };
 
 
-// The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1);
-// `sectors` (hash-chosen words, H < 4) is the launch's flag.
+// The H bits of one s-mer hash as eight 32-bit halves (word w -> halves 2w, 2w+1),
+// hash i in word i mod 4 (filters with hash-chosen sectors run the
+// runtime-parameter kernels).
 // kTable: the one-hot halves of a bit position come from a 64-entry shared
 // table (tab[p] = halves of 1 << p), one shared load instead of a variable
 // 64-bit shift on the ALU pipe (the query, ALU-bound, gains ~4 %; the insert
 // does not).
 template <int H, bool kTable>
-__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab, int sectors) {
+__device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab) {
     constexpr int SW = 64 / H;
 #pragma unroll
     for (int j = 0; j < 8; ++j) m[j] = 0u;
@@ -409,17 +404,6 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const ui
         uint32_t pos;
         if constexpr (SW >= 6) pos = (uint32_t)(hs >> (i * SW)) & 63u;
         else pos = (uint32_t)((hs * salt_of(i)) >> 58);
-        if (H < 4 && sectors) {
-            // hash-chosen sector (H < 4): the word is sector_word, not i mod 4
-            const uint32_t w = sector_word(hs, i, SW);
-            const uint64_t one = 1ull << pos;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                m[2 * q] |= w == (uint32_t)q ? (uint32_t)one : 0u;
-                m[2 * q + 1] |= w == (uint32_t)q ? (uint32_t)(one >> 32) : 0u;
-            }
-            continue;
-        }
         if constexpr (kTable) {
             const uint2 one = tab[pos];
             m[2 * (i & 3)] |= one.x;
@@ -432,7 +416,12 @@ __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const ui
     }
 }
 
-template <int K, int M, int S, int H, bool kQuery, int A = 0, int D = 0>
+// FQ = 1 (DNA insert only): finished runs leave through the warp's run queue
+// (queue_runs), one 32-byte request per run, instead of four 64-bit OR
+// reductions from the run's lane.  The library takes it for filters several
+// times larger than L2, where every run is a DRAM read-modify-write; it
+// costs instructions where the filter is cached.
+template <int K, int M, int S, int H, bool kQuery, int A = 0, int D = 0, int FQ = 0>
 __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(LaunchArgs a) {
     using C = StripCfg<K, M, S, H, A, D>;
     constexpr int W = C::W, Z = C::Z, NB = C::NB, L = C::L, NT = C::NT, TILE = C::TILE;
@@ -446,7 +435,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
     __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
     // DNA insert: per warp, a ring of finished runs (shard key, eight
     // half-words) that the warp drains four lanes per run
-    constexpr bool kQueue = !kQuery && A == 0;
+    constexpr bool kQueue = !kQuery && A == 0 && FQ;
     constexpr int QN = 64;
     __shared__ __align__(16) uint32_t fq_acc[kQueue ? (NT / 32) * QN * 8 : 1];
     __shared__ uint32_t fq_key[kQueue ? (NT / 32) * QN : 1];
@@ -779,14 +768,14 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                     codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
                     for (int z = 0; z < Z; ++z)
-                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot, a.sectors);
+                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
                 } else {
 #pragma unroll
                     for (int i = 0; i < S - 1; ++i) vb = (vb << BITS) | sm.pcode[kk0 + 16 + i];
 #pragma unroll
                     for (int z = 0; z < Z; ++z) {
                         vb = (vb << BITS) | sm.pcode[kk0 + 16 + z + S - 1];
-                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot, a.sectors);
+                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot);
                     }
 #pragma unroll
                     for (int i = 0; i < M - 1; ++i) va = (va << BITS) | sm.pcode[kk0 + 15 + i];
@@ -894,7 +883,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             vb = (vb << BITS) | sm.pcode[kb + 16 + Z + i + S - 1];
                             sv = vb & kMaskS;
                         }
-                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot, a.sectors);
+                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot);
                         // OR of the k-mer's older s-mers (its newest is mk[Z])
                         uint32_t older[8];
 #pragma unroll
@@ -908,15 +897,17 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             const uint32_t key = shard[i] | ((((uint32_t)(vwin >> i)) & 1u) ^ 1u) << 31;
                             // DNA (runs of ~(w+1)/2 = 8.5 k-mers): each lane flushes its own
                             // runs; protein (runs of ~3): the warp flushes cooperatively
-                            if constexpr (A == 0) {
+                            if constexpr (kQueue) {
                                 const bool fl = key != cur_key && !(cur_key >> 31);
                                 if (am == 0xffffffffu)
                                     queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head,
-                                                      q_tail, fl, cur_key, acc, tid & 31, 8, words, a.sectors);
+                                                      q_tail, fl, cur_key, acc, tid & 31, 8, words);
                                 else if (fl)
-                                    flush_run<H>(words + (uint64_t)cur_key * 4, acc, a.sectors);
+                                    flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                            } else if constexpr (A == 0) {
+                                if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                             } else {
-                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am, a.sectors);
+                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am);
                             }
                             const uint32_t same = key == cur_key ? 1u : 0u;
 #pragma unroll
@@ -962,15 +953,17 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                 }
             }
             if constexpr (!kQuery) {
-                if constexpr (A == 0) {
+                if constexpr (kQueue) {
                     // the strip's last runs, then everything still queued
                     if (am == 0xffffffffu)
                         queue_runs<H, QN>(fq_acc + (tid >> 5) * QN * 8, fq_key + (tid >> 5) * QN, q_head, q_tail,
-                                          !(cur_key >> 31), cur_key, acc, tid & 31, 1, words, a.sectors);
+                                          !(cur_key >> 31), cur_key, acc, tid & 31, 1, words);
                     else if (!(cur_key >> 31))
-                        flush_run<H>(words + (uint64_t)cur_key * 4, acc, a.sectors);
+                        flush_run<H>(words + (uint64_t)cur_key * 4, acc);
+                } else if constexpr (A == 0) {
+                    if (!(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                 } else {
-                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am, a.sectors);
+                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am);
                 }
             }
         }

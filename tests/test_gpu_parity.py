@@ -486,3 +486,36 @@ def test_runtime_kernels_flag_matches_strip_kernels(params):
         sbf.close()
     assert_images_equal(res[1][0], res[0][0])
     assert_words_equal(res[1][1], res[0][1], qoff)
+
+
+def test_queued_insert_on_a_filter_far_larger_than_l2():
+    """Filters several times larger than L2 insert with the warp run-queue
+    flush.  A 2^34-bit (2 GiB) filter takes it; the image must equal the
+    oracle's, with inputs that flush many runs per step (records of one or
+    two k-mers, N runs) and ragged warps at the batch's end."""
+    torch = need_gpu()
+    from minimizer_sharded_bloom_gb300 import SuperBloomFilter
+    rng = np.random.default_rng(4321)
+    long = synth.random_records(rng, 6, 5_000, 60_000, n_prob=0.002, lower_prob=0.01)
+    short = synth.random_records(rng, 3_000, 31, 33, n_prob=0.01)
+    tail = synth.random_records(rng, 37, 0, 900)
+    seq = np.concatenate([long.seq, short.seq, tail.seq])
+    off = np.concatenate([long.offsets, long.offsets[-1] + short.offsets[1:],
+                          long.offsets[-1] + short.offsets[-1] + tail.offsets[1:]])
+    sbf = SuperBloomFilter(1 << 34, seed=21, **MAIN)
+    assert sbf.specialized
+    gpu_insert(torch, sbf, seq, off)
+    assert sbf.status() == 0
+    img = sbf.to_tensor()
+    torch.cuda.synchronize()
+    sh, words = oracle.insert_sparse(seq, off, MAIN["k"], MAIN["m"], MAIN["s"], MAIN["H"], sbf.num_shards, 21)
+    nz = int((img != 0).any(dim=1).sum().item())
+    assert nz == sh.size
+    got = img.index_select(0, torch.from_numpy(sh.astype(np.int64)).cuda()).cpu().numpy().view(np.uint64)
+    assert np.array_equal(got, words)
+    # and the same batch answers present everywhere it has a valid k-mer
+    out = gpu_query(torch, sbf, seq, off)
+    want = oracle.query(np.zeros((1, 4), np.uint64) + np.uint64(2**64 - 1), seq, off, MAIN["k"], MAIN["m"],
+                        MAIN["s"], MAIN["H"], 21)
+    assert_words_equal(out, want, off)
+    sbf.close()
