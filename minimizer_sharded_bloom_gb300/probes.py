@@ -138,3 +138,45 @@ def read_rate(torch, mode: str = "ld_nc", gib: int = 8, n_reads: int = 100_000_0
         torch.cuda.empty_cache()
     return {"mode": mode, "rows_per_s": n_reads / t, "ms": 1e3 * t, "buffer_gib": n_rows * 32 / 2**30,
             "reads": n_reads}
+
+
+def launch_each_once(torch, gib: int = 2, rows: int = 25_000_000) -> None:
+    """One launch of every memory probe (each RMW and read form) over a gib-GiB
+    buffer, rows rows each: the command a counter capture (ncu) profiles."""
+    L = load()
+    buf = torch.zeros((gib << 30) // 8, dtype=torch.int64, device="cuda")
+    blocks = sm_count() * 8
+    sink = torch.empty(blocks * 256, dtype=torch.int64, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    for name, mode in RMW_MODES.items():
+        _check(L.sbf_probe_rmw(mode, buf.data_ptr(), buf.numel() // 4, rows, 12345 + mode, blocks, 256, st), name)
+    for name, mode in READ_MODES.items():
+        _check(L.sbf_probe_read(mode, buf.data_ptr(), buf.numel() // 4, rows, 777 + mode, blocks, 256,
+                                sink.data_ptr(), st), name)
+    torch.cuda.synchronize()
+
+
+def main(argv=None) -> None:
+    """python -m minimizer_sharded_bloom_gb300.probes [--once]: every probe's
+    rate as one JSON line (8 GiB buffer, 118 M rows), or, with --once, one
+    launch of each memory probe for a counter capture."""
+    import argparse
+    import json
+    import torch
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--once", action="store_true")
+    args = ap.parse_args(argv)
+    build_lib.build()
+    torch.cuda.set_device(0)
+    if args.once:
+        launch_each_once(torch)
+        return
+    out = {"sms": sm_count(), "alu": [alu_rate(torch, k) for k in ALU_KINDS]}
+    buf = torch.zeros((8 << 30) // 8, dtype=torch.int64, device="cuda")
+    out["rmw"] = [rmw_rate(torch, m, n_updates=118_000_000, buf=buf) for m in RMW_MODES]
+    out["read"] = [read_rate(torch, m, n_reads=118_000_000, buf=buf) for m in READ_MODES]
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()
