@@ -126,15 +126,22 @@ def alu_ops(p):
 # probe rate is the pattern ceiling the insert and query are reported against:
 # the DNA insert flushes a run with four 64-bit OR reductions from its lane
 # ("red4"), or, on filters larger than 8x the L2 (where the library takes the
-# queued insert), through its warp's run queue ("red_queue"); the query copies
+# queued insert), through its warp's run queue ("red_queue"; the protein and
+# triplet inserts' cooperative flush is of that form too); the query copies
 # each run head's shard with two 16-byte cp.async.cg.
 QUEUED_INSERT_L2_MULTIPLE = 8
 QUERY_SHARD_FORM = "cp_async"
 
 
 def insert_flush_form(torch, filter_bits: int, alphabet: str) -> str:
+    """The RMW probe form of the insert's run flush: the protein and triplet
+    strip kernels flush a warp's runs cooperatively (one 32-byte request per
+    run, like the queue); DNA queues them on filters larger than 8x the L2 and
+    otherwise sends four reductions from the run's lane."""
+    if alphabet != "dna":
+        return "red_queue"
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-    if alphabet == "dna" and filter_bits // 8 > QUEUED_INSERT_L2_MULTIPLE * l2:
+    if filter_bits // 8 > QUEUED_INSERT_L2_MULTIPLE * l2:
         return "red_queue"
     return "red4"
 
