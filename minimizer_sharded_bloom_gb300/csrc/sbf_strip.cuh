@@ -29,7 +29,8 @@
 //    k-mer's four word masks and inserts or tests them.  For query, pass A
 //    copies each run head's 32-byte shard into shared memory (cp.async), so
 //    the shard is on chip by the time pass B reads it (Sec. IV-E/IV-G: one
-//    256-bit load per shard).
+//    256-bit load per shard); heads beyond the block's slots get an L2
+//    prefetch instead, and pass B loads them directly.
 //
 //  * Runs (Fig. 3): consecutive k-mers of a strip with one shard form a run;
 //    their masks are ORed in registers and the run issues one 64-bit atomic OR
@@ -832,10 +833,12 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                                                            : (shard[i] != shard[i - 1]);
                                 if (head) {
                                     heads |= 1u << i;
+                                    const uint64_t *src = words + (uint64_t)shard[i] * 4;
                                     if (nh < R) {
-                                        const uint64_t *src = words + (uint64_t)shard[i] * 4;
                                         cp_async16(smem_u32(&slot_mem[(nh * 2 + 0) * NT + tid]), src);
                                         cp_async16(smem_u32(&slot_mem[(nh * 2 + 1) * NT + tid]), src + 2);
+                                    } else {
+                                        prefetch_l2(src);
                                     }
                                     ++nh;
                                 }
@@ -852,10 +855,12 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                                                    : (shard[W - 1] != shard[W > 1 ? W - 2 : 0]);
                         if (head) {
                             heads |= 1u << (W - 1);
+                            const uint64_t *src = words + (uint64_t)shard[W - 1] * 4;
                             if (nh < R) {
-                                const uint64_t *src = words + (uint64_t)shard[W - 1] * 4;
                                 cp_async16(smem_u32(&slot_mem[(nh * 2 + 0) * NT + tid]), src);
                                 cp_async16(smem_u32(&slot_mem[(nh * 2 + 1) * NT + tid]), src + 2);
+                            } else {
+                                prefetch_l2(src);
                             }
                         }
                     }
@@ -934,9 +939,11 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             uint32_t miss = 0u;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) miss |= (older[j] | mk[Z][j]) & ~f[j];
-                            present |= (uint32_t)(((vwin >> i) & 1u) && miss == 0u) << i;
+                            present |= (miss == 0u ? 1u : 0u) << i;
                         }
                     }
+                    // only valid k-mers answer (one AND for the block)
+                    if (kQuery) present &= (uint32_t)vwin & (W >= 32 ? 0xFFFFFFFFu : ((1u << W) - 1u));
                     if (kQuery && present) {
                         if constexpr (A == 2) {
                             // k-mer kb + i starts at tile byte pass + 3 (kb + i)
