@@ -115,43 +115,57 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
 }
 
 // Per-warp queue of finished runs (DNA insert).  A lane whose run ends
-// writes it (shard key, eight half-words) at the queue's tail; once
-// drain_at runs wait, the warp drains them in groups of eight, lane l
-// reducing word l & 3 of run l >> 2, so that each run's four words reach L2
-// as one 32-byte request instead of four (drain_at = 1: drain everything,
-// the last group partly).  head / tail are warp-uniform counters; the ring
-// holds QN = 64 entries (with drain_at <= 32, at most 31 wait after a drain
-// and a step adds at most 32).  Called by all 32 lanes.
+// writes it (shard key, eight half-words) at the queue's tail; once drain_at
+// runs wait, the warp drains them in groups of eight, lane l reducing word
+// l & 3 of run l >> 2, so that each run's four words reach L2 as one 32-byte
+// request instead of four (drain_at = 1: the strip's end, everything, the
+// last group partly).  head / tail are warp-uniform counters.  The ring holds
+// QN = 128 entries: at most 39 runs wait when a drain starts (7 left over plus
+// one step's 32), so the next step's writes land at least 128 - 2 * 39 slots
+// away from the entries a drain just read, and the warp need not synchronise
+// after a drain; it does before one (the entries it reads were written by
+// other lanes).  Called by all 32 lanes.
+template <int H, int QN>
+__device__ __forceinline__ void drain_group(const uint32_t *q_acc, const uint32_t *q_key, int head, int lane,
+                                            uint64_t *words) {
+    const int e = (head + (lane >> 2)) & (QN - 1), wd = lane & 3;
+    const uint2 v = reinterpret_cast<const uint2 *>(q_acc + 8 * e)[wd];
+    const uint64_t x = ((uint64_t)v.y << 32) | v.x;
+    if (wd < H && x)
+        asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)q_key[e] * 4 + wd), "l"(x) : "memory");
+}
+
 template <int H, int QN>
 __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int &head, int &tail, bool flush,
                                            uint32_t key, const uint32_t acc[8], int lane, int drain_at,
                                            uint64_t *words) {
     const unsigned fm = __ballot_sync(0xffffffffu, flush);
-    if (fm) {
-        if (flush) {
-            const int e = (tail + __popc(fm & ((1u << lane) - 1u))) & (QN - 1);
-            q_key[e] = key;
-            uint4 *d = reinterpret_cast<uint4 *>(q_acc + 8 * e);
-            d[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
-            d[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        tail += __popc(fm);
+    const unsigned lt = (1u << lane) - 1u;
+    const int e = (tail + __popc(fm & lt)) & (QN - 1);
+    if (flush) {
+        q_key[e] = key;
+        uint4 *d = reinterpret_cast<uint4 *>(q_acc + 8 * e);
+        d[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        d[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
     }
-    if (tail - head >= drain_at) {
+    tail += __popc(fm);
+    if (drain_at > 1) {
+        // during the strip: whole groups of eight only
+        if (tail - head >= drain_at) {
+            __syncwarp();
+            do {
+                drain_group<H, QN>(q_acc, q_key, head, lane, words);
+                head += 8;
+            } while (tail - head >= 8);
+        }
+    } else if (tail > head) {
+        // the strip's end: everything, the last group partly
         __syncwarp();
-        const int wd = lane & 3;
         do {
-            if (head + (lane >> 2) < tail) {
-                const int e = (head + (lane >> 2)) & (QN - 1);
-                const uint2 v = reinterpret_cast<const uint2 *>(q_acc + 8 * e)[wd];
-                const uint64_t x = ((uint64_t)v.y << 32) | v.x;
-                if (wd < H && x)
-                    asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)q_key[e] * 4 + wd), "l"(x)
-                                 : "memory");
-            }
+            if (head + (lane >> 2) < tail) drain_group<H, QN>(q_acc, q_key, head, lane, words);
             head += 8;
-        } while (tail - head >= (drain_at > 1 ? 8 : 1));
-        if (head > tail) head = tail;
+        } while (tail > head);
+        head = tail;
         __syncwarp();
     }
 }
@@ -393,8 +407,8 @@ struct StripSmem {
 // runtime-parameter kernels).
 // kTable: the one-hot halves of a bit position come from a 64-entry shared
 // table (tab[p] = halves of 1 << p), one shared load instead of a variable
-// 64-bit shift on the ALU pipe (the query, ALU-bound, gains ~4 %; the insert
-// does not).
+// 64-bit shift on the ALU pipe (the query and the queued insert gain ~4 % and
+// ~1 %; the direct insert on a cached filter loses ~3 % and keeps the shifts).
 template <int H, bool kTable>
 __device__ __forceinline__ void smer_halves(uint64_t hs, uint32_t m[8], const uint2 *tab) {
     constexpr int SW = 64 / H;
@@ -434,10 +448,10 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
     __shared__ StripSmem<K, M, S, H, A, D> sm;
     // query: shards of the current block's run heads, [slot][half][thread]
     __shared__ __align__(16) uint4 slot_mem[kQuery ? R * 2 * NT : 1];
-    // DNA insert: per warp, a ring of finished runs (shard key, eight
-    // half-words) that the warp drains four lanes per run
+    // DNA insert with FQ = 1: per warp, a ring of finished runs (shard key,
+    // eight half-words) that the warp drains four lanes per run
     constexpr bool kQueue = !kQuery && A == 0 && FQ;
-    constexpr int QN = 64;
+    constexpr int QN = 128;
     __shared__ __align__(16) uint32_t fq_acc[kQueue ? (NT / 32) * QN * 8 : 1];
     __shared__ uint32_t fq_key[kQueue ? (NT / 32) * QN : 1];
 
@@ -492,7 +506,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         sm.abort_flag = 0;
     }
 
-    if (kQuery && tid < 64)
+    if ((kQuery || kQueue) && tid < 64)
         sm.onehot[tid] = make_uint2(tid < 32 ? 1u << tid : 0u, tid >= 32 ? 1u << (tid - 32) : 0u);
     __syncthreads();
     uint32_t raw_phase = 0;
@@ -769,14 +783,14 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                     codes64_at(sm.codes, kk0 + 16, wv);
 #pragma unroll
                     for (int z = 0; z < Z; ++z)
-                        smer_halves<H, kQuery>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
+                        smer_halves<H, kQuery || kQueue>(hash_smer(win_value(wv, z, S), seed_s), mk[z + 1], sm.onehot);
                 } else {
 #pragma unroll
                     for (int i = 0; i < S - 1; ++i) vb = (vb << BITS) | sm.pcode[kk0 + 16 + i];
 #pragma unroll
                     for (int z = 0; z < Z; ++z) {
                         vb = (vb << BITS) | sm.pcode[kk0 + 16 + z + S - 1];
-                        smer_halves<H, kQuery>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot);
+                        smer_halves<H, kQuery || kQueue>(hash_smer(vb & kMaskS, seed_s), mk[z + 1], sm.onehot);
                     }
 #pragma unroll
                     for (int i = 0; i < M - 1; ++i) va = (va << BITS) | sm.pcode[kk0 + 15 + i];
@@ -888,7 +902,7 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             vb = (vb << BITS) | sm.pcode[kb + 16 + Z + i + S - 1];
                             sv = vb & kMaskS;
                         }
-                        smer_halves<H, kQuery>(hash_smer(sv, seed_s), mk[Z], sm.onehot);
+                        smer_halves<H, kQuery || kQueue>(hash_smer(sv, seed_s), mk[Z], sm.onehot);
                         // OR of the k-mer's older s-mers (its newest is mk[Z])
                         uint32_t older[8];
 #pragma unroll
