@@ -114,6 +114,19 @@ __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const 
     }
 }
 
+// A run head's shard in pass B: from its slot when `staged`, else straight
+// from global memory (64-byte L2 fetch), chosen by predicate inside one asm
+// block rather than by a nested branch.
+__device__ __forceinline__ void head_shard(uint64_t &a, uint64_t &b, uint64_t &c, uint64_t &d, uint32_t lo,
+                                           uint32_t hi, const uint64_t *src, bool staged) {
+    asm volatile("{ .reg .pred q; setp.ne.u32 q, %4, 0;\n\t"
+                 "@q ld.shared.v2.u64 {%0, %1}, [%5];\n\t@q ld.shared.v2.u64 {%2, %3}, [%6];\n\t"
+                 "@!q ld.global.nc.L2::64B.v4.u64 {%0, %1, %2, %3}, [%7]; }"
+                 : "=l"(a), "=l"(b), "=l"(c), "=l"(d)
+                 : "r"(staged ? 1u : 0u), "r"(lo), "r"(hi), "l"(src)
+                 : "memory");
+}
+
 // Per-warp queue of finished runs (DNA insert).  A lane whose run ends
 // writes it (shard key, eight half-words) at the queue's tail; once drain_at
 // runs wait, the warp drains them in groups of eight, lane l reducing word
@@ -168,16 +181,6 @@ __device__ __forceinline__ void queue_runs(uint32_t *q_acc, uint32_t *q_key, int
         head = tail;
         __syncwarp();
     }
-}
-
-// One 256-bit shard through the non-coherent path (Sec. IV-G).  The L2
-// fetches 64 bytes around it instead of its default 128-byte line: scattered
-// shards gain nothing from the larger fetch (same rate, twice the DRAM bytes).
-__device__ __forceinline__ void load_shard(const uint64_t *p, uint64_t &a, uint64_t &b, uint64_t &c,
-                                           uint64_t &d) {
-    asm volatile("ld.global.nc.L2::64B.v4.u64 {%0, %1, %2, %3}, [%4];"
-                 : "=l"(a), "=l"(b), "=l"(c), "=l"(d)
-                 : "l"(p));
 }
 
 // 16 ASCII bytes (w[0] holds bytes 0..3, little-endian) -> 16 2-bit codes with
@@ -935,16 +938,10 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                         } else {
                             if (i == W - 1) cp_async_wait<0>();
                             if ((heads >> i) & 1u) {
-                                if (nb < R) {
-                                    const uint4 lo4 = slot_mem[(nb * 2 + 0) * NT + tid];
-                                    const uint4 hi4 = slot_mem[(nb * 2 + 1) * NT + tid];
-                                    F0 = ((uint64_t)lo4.y << 32) | lo4.x;
-                                    F1 = ((uint64_t)lo4.w << 32) | lo4.z;
-                                    F2 = ((uint64_t)hi4.y << 32) | hi4.x;
-                                    F3 = ((uint64_t)hi4.w << 32) | hi4.z;
-                                } else {
-                                    load_shard(words + (uint64_t)shard[i] * 4, F0, F1, F2, F3);
-                                }
+                                const int sl = nb < R ? nb : R - 1;
+                                head_shard(F0, F1, F2, F3, smem_u32(&slot_mem[(sl * 2 + 0) * NT + tid]),
+                                           smem_u32(&slot_mem[(sl * 2 + 1) * NT + tid]),
+                                           words + (uint64_t)shard[i] * 4, nb < R);
                                 ++nb;
                             }
                             const uint32_t f[8] = {(uint32_t)F0, (uint32_t)(F0 >> 32), (uint32_t)F1,
