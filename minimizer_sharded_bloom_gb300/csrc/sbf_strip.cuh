@@ -396,6 +396,7 @@ struct StripSmem {
     uint32_t frame[A == 2 ? C::BIT_WORDS : 1];
     int64_t prev_start;
     int scan_tmp[4];
+    uint32_t need_tmp[4];               // triplets: per warp, residues mod 3 of the boundaries
     uint2 onehot[64];                   // halves of 1 << p, p = 0 .. 63
     uint64_t raw_bar;                                   // completes the raw bulk copy
     int abort_flag;
@@ -670,15 +671,27 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
             const int lane = tid & 31, warp = tid >> 5;
             int loc[PER];
             int run = -1;
+            // a symbol of pass p (byte b = p + 3c) is in frame after a boundary at
+            // byte lb iff p = lb mod 3; bit r of `res`: a boundary with lb mod 3 = r
+            uint32_t res = 0u;
 #pragma unroll
             for (int j = 0; j < PER; ++j) {
                 const int w = tid * PER + j;
                 if (w < C::BYTE_WORDS) {
                     const uint32_t x = sm.bstarts[w];
-                    if (x) run = 32 * w + 31 - __clz(x);
+                    if (x) {
+                        run = 32 * w + 31 - __clz(x);
+                        // bit i of word w is byte 32 w + i, = 2 w + i mod 3
+                        const uint32_t cls = ((x & 0x49249249u) ? 1u : 0u) | ((x & 0x92492492u) ? 2u : 0u) |
+                                             ((x & 0x24924924u) ? 4u : 0u);
+                        const int sh = (2 * w) % 3;
+                        res |= ((cls << sh) | (cls >> (3 - sh))) & 7u;
+                    }
                 }
                 loc[j] = run;
             }
+            res = __reduce_or_sync(0xffffffffu, res);
+            if (lane == 0) sm.need_tmp[warp] = res;
             int incl = run;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -701,6 +714,18 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
         }
 
         for (int pass = 0; pass < NPASS; ++pass) {
+        if constexpr (A == 2) {
+            // a pass none of whose symbols is in frame holds no valid k-mer and
+            // is skipped (block-uniform): pass p is in frame after a boundary
+            // at byte lb iff p = lb mod 3 (need_tmp), and before the tile's
+            // first boundary iff p + prev_res = 0 mod 3
+            const uint32_t need = sm.need_tmp[0] | sm.need_tmp[1] | sm.need_tmp[2] | sm.need_tmp[3] |
+                                  (prev_res >= 0 ? 1u << ((3 - prev_res) % 3) : 0u);
+            if (!((need >> pass) & 1u)) {
+                if (pass == NPASS - 1) next_copy();
+                continue;
+            }
+        }
         if constexpr (A == 2) {
             // ---- phase 2 (triplets): symbol c of this pass is the codon at byte
             // b = pass + 3c; invalid if a base is invalid or a record boundary
