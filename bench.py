@@ -153,7 +153,7 @@ def insert_flush_form(torch, filter_bits: int, alphabet: str) -> str:
 # where each run costs one DRAM read-modify-write of its shard at either
 # size (the earlier full-size and profiling-size captures agreed within 3 %).
 MEASURED_TRAFFIC = {
-    "out-of-cache": {"source_sha": "cc69497f99512991", "insert": 14.1358, "query": 9.6950},
+    "out-of-cache": {"source_sha": "38e81bcbf7a94f54", "insert": 14.1490, "query": 9.7807},
 }
 
 def kernel_source_sha(p=MAIN) -> str:
@@ -658,11 +658,26 @@ def measure_ceilings(torch, filter_bits: int, small: bool = False) -> dict:
     return res
 
 
-def _timed(torch, fn, warmup=2, reps=3):
+def _timed(torch, fn, warmup=2, reps=3, before=None):
+    """Seconds per call of `fn`: the mean of `reps` back-to-back calls, or, with
+    `before` (run untimed ahead of every call, e.g. zeroing the filter), the
+    median of `reps` calls each bracketed by its own events."""
     for _ in range(warmup):
+        if before is not None:
+            before()
         fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if before is not None:
+        times = []
+        for _ in range(reps):
+            before()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) / 1e3)
+        return statistics.median(times)
     e0.record()
     for _ in range(reps):
         fn()
@@ -695,8 +710,10 @@ def run_suite(args):
         di, dio = dev(ins)
         dq, dqo = dev(qry)
         out = torch.zeros((qry.n_bases + 31) // 32 + 2, dtype=torch.int32, device="cuda")
+        # the filter is zeroed before every timed insert, as in the main bench
         t_ins = _timed(torch, lambda: N.sbf_insert(sbf.handle, di.data_ptr(), dio.data_ptr(),
-                                                    ins.n_records, st))
+                                                    ins.n_records, st),
+                       reps=5, before=lambda: N.sbf_clear(sbf.handle, st))
         t_q = _timed(torch, lambda: N.sbf_query(sbf.handle, dq.data_ptr(), dqo.data_ptr(),
                                                  qry.n_records, out.data_ptr(), st))
         words = out.cpu().numpy().view(np.uint32)
