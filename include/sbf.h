@@ -167,7 +167,7 @@ int sbf_query(const sbf_filter *f, const char *seq, const int64_t *offsets, int6
  * when the device can access it -- pageable-memory access through the host
  * page tables (Grace systems over NVLink-C2C) -- with no copies.  Otherwise
  * (or after sbf_set_host_mode(f, 1)) the records are staged to the device in
- * chunks on four rotating streams, overlapping copies with kernels (Sec. IV-G,
+ * chunks on eight rotating streams, overlapping copies with kernels (Sec. IV-G,
  * host FASTX staging): page-locked buffers are copied from directly, pageable
  * ones through pinned staging buffers.  Chunks end at record starts where possible; a record
  * longer than a chunk is cut, with the k-1 bytes of overlap its k-mers need.
@@ -216,7 +216,7 @@ int sbf_query_host_noalloc(const sbf_filter *f, const char *seq, const int64_t *
  * 2 reads in place whenever the device can. */
 int sbf_set_host_mode(sbf_filter *f, int mode);
 
-/* Largest chunk of the staged host-facing calls, in sequence positions (default 2^26;
+/* Largest chunk of the staged host-facing calls, in sequence positions (default 2^25;
  * rounded down to a multiple of 32; at least 32).  A call cuts its batch into
  * chunks of up to about an eighth of it, at least 2^22 positions and at most this
  * setting; the first chunks are smaller (from 2^22 positions, doubling).

@@ -46,10 +46,14 @@ struct Slot {
     int64_t pend_words = 0;
 };
 
+constexpr int kSlots = 8;
+
 struct Stager {
-    // four slots: a chunk's copy waits only for the chunk four back, which
-    // leaves the copy engine slack when copies and kernels take about as long
-    Slot slot[4];
+    // kSlots slots: a chunk's copy waits only for the chunk kSlots back,
+    // which leaves the copy engine slack when copies and kernels take about
+    // as long, and keeps the batch's small last chunks from waiting on the
+    // kernels of its large middle ones
+    Slot slot[kSlots];
     int64_t *d_all_off = nullptr;  // the whole offsets array of a call, on the device
     int64_t cap_all_off = 0;
     int *d_call_flag = nullptr;    // its uniformity flag (from the one check of the call)
@@ -141,7 +145,7 @@ const void *device_alias(const void *p, int dev) {
 // Returns 1 when done this way, 0 when the buffers are not device-accessible.
 int run_in_place(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint32_t *out_bits,
                  void *user_stream, bool query, int *rc) {
-    const int64_t lo = off[0], hi = off[n];
+    const int64_t lo = off[0];
     const void *s_al = device_alias(seq + lo, f->device);
     const void *o_al = device_alias(off, f->device);
     const void *q_al = query ? device_alias(out_bits + (lo >> 5), f->device) : nullptr;
@@ -291,7 +295,7 @@ int run_host(sbf_filter *f, const char *seq, const int64_t *off, int64_t n, uint
         const int64_t n_loc = r1 - r0;
         const int64_t dev_words = (data_hi - cs + 31) / 32 + 1;  // what the kernel may write
         const int64_t words = (ce - cs + 31) / 32;                // what this chunk returns
-        Slot &s = st.slot[c % 4];
+        Slot &s = st.slot[c % kSlots];
         if (s.stream && host_staging) {
             if (cudaStreamSynchronize(s.stream) != cudaSuccess) {
                 rc = set_error(SBF_ERR_CUDA, "staging stream failed");

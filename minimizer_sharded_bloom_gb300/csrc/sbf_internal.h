@@ -31,7 +31,7 @@ struct sbf_filter {
     bool runtime_requested = false;  // SBF_FLAG_RUNTIME_KERNELS given at creation
     bool strip = false;         // insert/query kernels are strip kernels (bounded mbarrier waits)
     void *stager = nullptr;     // host-facing staging buffers, created on first use
-    int64_t host_chunk = int64_t(1) << 26;  // host-facing chunk, in positions
+    int64_t host_chunk = int64_t(1) << 25;  // host-facing chunk, in positions
     int host_mode = 0;          // 0: read host buffers in place when possible; 1: always stage
 };
 
