@@ -6,17 +6,19 @@
 // GB300:
 //
 //  * Tile front end (Sec. IV-C): a CTA owns TILE consecutive k-mer positions.
-//    It reads the TILE + k bases it needs once, as 16-byte coalesced loads,
-//    converts 16 bytes at a time to 2-bit codes (first base in the high bits)
-//    plus an invalid-byte bitmap with SWAR byte arithmetic, marks record starts
-//    from the CSR offsets, and derives one validity bit per k-mer with
-//    bit-parallel window ORs.  Everything lives in shared memory.
+//    The TILE + k bytes it needs arrive once, by one TMA bulk copy issued a
+//    tile ahead (16-byte loads where the copy cannot be used); 16 bytes at a
+//    time become 2-bit codes (first base in the high bits) plus an
+//    invalid-byte bitmap with SWAR byte arithmetic; record starts come from
+//    the CSR offsets (or arithmetically for dense batches), and one validity
+//    bit per k-mer from bit-parallel window ORs.  Everything lives in shared
+//    memory.
 //
 //  * Strips instead of one k-mer per thread (Sec. IV-E amortises packing over
 //    kStride = 4 k-mers; here every thread owns a strip of L = NB*w
-//    consecutive k-mers).  Bases enter a rolling register one at a time, so
-//    each m-mer and each s-mer is packed and hashed once, not once per k-mer
-//    that contains it.
+//    consecutive k-mers).  Each m-mer and each s-mer is cut out of a 64-base
+//    window of the code tile by funnel shifts and hashed once, not once per
+//    k-mer that contains it.
 //
 //  * Minimizer (Algorithm 1's minimum m-mer hash) with a Gil-Werman / van Herk sliding
 //    minimum: the m-mer hashes are cut into blocks of w = k-m+1; the minimum
@@ -36,6 +38,9 @@
 //    their masks are ORed in registers and the run issues one 64-bit atomic OR
 //    (a fire-and-forget reduction) per non-zero word -- the paper's segmented
 //    warp reduction happens inside the thread, where the super-k-mer lies.
+//    On filters far larger than L2 (FQ = 1) finished runs go through a
+//    per-warp shared-memory queue instead, drained four lanes per run, so a
+//    run's four words reach L2 as one 32-byte request.
 //
 // Shared-memory indexing: code index ci <-> absolute base position
 // T0 - 16 + ci, where T0 (a multiple of 32) is the tile's first k-mer; the
@@ -47,7 +52,10 @@
 // B roll their m-mer / s-mer values forward by one symbol per position
 // (v = v << 5 | code) instead of cutting them out of 64-base windows.  Validity,
 // record starts, the sliding minimum, runs and the query's shard slots are the
-// same code.
+// same code.  A = 2 is the DNA-triplet alphabet (6-bit codons read in frame):
+// a tile covers three times the bytes, in up to three frame passes that each
+// form one codon per three bytes and then run the protein machinery; a pass
+// with no codon in frame is skipped.
 #pragma once
 
 #include <cstdint>

@@ -63,3 +63,14 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "k-mers/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_kernel_hash_sees_code_not_comments():
+    """The stored DRAM traffic is keyed by a hash of the kernels' code: comments
+    and layout leave it as it is, any change of a token changes it."""
+    src = "int a = 1; // one\n/* block\n comment */ int  b =\n 2;\n"
+    assert bench.code_only(src) == "int a = 1; int b = 2;"
+    assert bench.code_only(src.replace("// one", "// another note")) == bench.code_only(src)
+    assert bench.code_only(src.replace("b =", "c =")) != bench.code_only(src)
+    stored = bench.MEASURED_TRAFFIC["out-of-cache"]["source_sha"]
+    assert len(stored) == 16 and len(bench.kernel_source_sha()) == 16
