@@ -114,6 +114,45 @@ def test_protein_strip_kernel_mixed(torch, case):
                pad_front=3 * (case % 2))
 
 
+def _triplet_batch(rng, case):
+    """Record layouts that reach every branch of the triplet kernel's frame-pass
+    skip: boundaries of all three residues mod 3 in one tile (ragged lengths),
+    one residue only (lengths a multiple of 3, after a lead that is not), a
+    residue that turns every record (lengths = 1 mod 3), tiles with no boundary
+    at all (records longer than a 23 kB tile), and empty and 1-2 byte records."""
+    if case == 0:
+        return _records(rng, "dna_triplet", 2500, 0, 400, 1)
+    if case == 1:
+        body = _records(rng, "dna_triplet", 3000, 150, 150, 0)
+        lead = 77
+        return synth.Workload(np.concatenate([np.full(lead, ord("C"), np.uint8), body.seq]),
+                              np.concatenate([[lead], lead + body.offsets[1:]]))
+    if case == 2:
+        return _records(rng, "dna_triplet", 2000, 151, 151, 1)
+    if case == 3:
+        return _records(rng, "dna_triplet", 12, 25_000, 70_000, 1)
+    if case == 4:
+        long = _records(rng, "dna_triplet", 6, 30_000, 50_000, 0)
+        short = _records(rng, "dna_triplet", 1500, 0, 2, 0)
+        return synth.Workload(np.concatenate([long.seq, short.seq, long.seq]),
+                              np.concatenate([long.offsets, long.offsets[-1] + short.offsets[1:],
+                                              long.offsets[-1] + short.offsets[-1] + long.offsets[1:]]))
+    return _records(rng, "dna_triplet", 600, 0, 2000, 2)
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_triplet_strip_kernel_mixed(torch, case):
+    """The triplet point runs the strip kernel (three frame passes per tile, a
+    pass with no codon in frame skipped by the whole block): tens of tiles of
+    the layouts of _triplet_batch, inserted and queried, on aligned (bulk-copied
+    tiles) and unaligned (direct loads) sequence pointers."""
+    rng = np.random.default_rng(7700 + case)
+    ins = _triplet_batch(rng, case)
+    qry = _with_own(ins, _triplet_batch(np.random.default_rng(7800 + case), (case + 1) % 6))
+    _roundtrip(torch, "dna_triplet", ins, qry, TRIPLET, [1 << 12, 1 << 16, 1 << 20, 1 << 22, 1 << 24, 1 << 18][case],
+               seed=int(rng.integers(0, 2**62)), pad_front=3 * (case % 2))
+
+
 @pytest.mark.parametrize("alphabet", ["protein", "dna_triplet"])
 def test_edge_cases(torch, alphabet):
     """n = 0 (no work, output untouched); only empty records; records shorter
