@@ -250,7 +250,7 @@ int64_t sbf_fastx_pending_bases(const sbf_fastx *r);
 
 void sbf_fastx_close(sbf_fastx *r); /* NULL-safe */
 
-/* 1 if this build reads gzip input, else 0. */
+/* 1 if the library was compiled with zlib and reads gzip input, else 0. */
 int sbf_fastx_has_gzip(void);
 
 /* Insert every record of a FASTA/FASTQ file through sbf_insert_host, in
