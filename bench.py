@@ -273,19 +273,29 @@ def runs_estimate(wl, k=K, m=M, B=1):
     return kmer_count(wl, k, B) * 2.0 / (w + 1) + wl.n_records
 
 
-def exact_runs(workload: str, role: str, wl, p, bits, k=K, m=M, B=1):
-    """(runs, source): the oracle's exact run count of this input (stored in
-    oracle/run_counts.json by oracle/run_counts.py, matched by the input's
-    fingerprint and parameters), else the 2/(w+1) estimate."""
+def stored_count(workload: str, role: str, wl, p, bits):
+    """The oracle's counts of this input (valid k-mers, runs, ...) from
+    oracle/run_counts.json, or None when no stored entry matches its
+    fingerprint and parameters."""
     try:
         with open(os.path.join(ROOT, "oracle", "run_counts.json")) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
-        rec = None
-    if rec and role in rec and rec.get("filter_bits") == bits and all(rec.get(x) == p[x] for x in ("k", "m", "s", "H")) \
-            and rec.get("alphabet") == p["alphabet"] and rec.get("seed") == SEED \
-            and rec[role]["fingerprint"] == synth.fingerprint(wl.seq, wl.offsets):
-        return float(rec[role]["runs"]), "exact (oracle run count of this input)"
+        return None
+    if not (rec and role in rec and rec.get("filter_bits") == bits
+            and all(rec.get(x) == p[x] for x in ("k", "m", "s", "H"))
+            and rec.get("alphabet") == p["alphabet"] and rec.get("seed") == SEED):
+        return None
+    return rec[role] if rec[role]["fingerprint"] == synth.fingerprint(wl.seq, wl.offsets) else None
+
+
+def exact_runs(workload: str, role: str, wl, p, bits, k=K, m=M, B=1):
+    """(runs, source): the oracle's exact run count of this input (stored in
+    oracle/run_counts.json by oracle/run_counts.py, matched by the input's
+    fingerprint and parameters), else the 2/(w+1) estimate."""
+    rec = stored_count(workload, role, wl, p, bits)
+    if rec:
+        return float(rec["runs"]), "exact (oracle run count of this input)"
     return runs_estimate(wl, k, m, B), "estimate 2/(w+1) per k-mer + 1 per record (no stored count matches)"
 
 
@@ -444,7 +454,15 @@ def main():
     p = spec.get("p", MAIN)
     B = sym_bytes(p)
     ins, qry = spec["make"]()
-    nk_ins, nk_q = kmer_count(ins, p["k"], B), kmer_count(qry, p["k"], B)
+    # k-mers/s counts valid k-mers: the oracle's count of this input where a
+    # stored one matches (the k-mer positions of clean records are all valid)
+    pos_ins, pos_q = kmer_count(ins, p["k"], B), kmer_count(qry, p["k"], B)
+    st_ins = stored_count(args.workload, "insert", ins, p, spec["bits"])
+    st_q = stored_count(args.workload, "query", qry, p, spec["bits"])
+    nk_ins = st_ins["valid_kmers"] if st_ins else pos_ins
+    nk_q = st_q["valid_kmers"] if st_q else pos_q
+    kmers_counted = ("valid k-mers (the oracle's count of this input)" if st_ins and st_q
+                     else "k-mer positions (no stored oracle count of this input)")
 
     dseq = torch.from_numpy(ins.seq).cuda()
     doff = torch.from_numpy(ins.offsets).cuda()
@@ -617,6 +635,12 @@ def main():
             "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
                        "alphabet": p["alphabet"], "seed": SEED,
                        "filter_bits": spec["bits"], "insert_kmers": nk_ins, "query_kmers": nk_q,
+                       "kmers_counted": kmers_counted,
+                       "insert_bases": int(ins.offsets[-1] - ins.offsets[0]),
+                       "query_bases": int(qry.offsets[-1] - qry.offsets[0]),
+                       "insert_kmer_positions": pos_ins, "query_kmer_positions": pos_q,
+                       "insert_valid_kmers": st_ins["valid_kmers"] if st_ins else None,
+                       "query_valid_kmers": st_q["valid_kmers"] if st_q else None,
                        "insert_records": n_ins, "query_records": n_q,
                        "l2": {"out-of-cache": "inputs larger than L2 (sequences 1 GB each, filter 8 GiB)",
                               "protein-like": "inputs larger than L2 (sequences 0.5 GB each, filter 1 GiB)",
@@ -752,11 +776,18 @@ def run_suite(args):
             del ones
         else:
             fpr, n_fpr = fpr_of(words, fq, k, B), fpr_count(fq, k, B)
+        # valid k-mers where the oracle's count of this input is stored, else positions
+        pp = dict(k=k, m=m, s=s, H=H, alphabet=alphabet)
+        st_i = stored_count(name, "insert", ins, pp, bits) if sectors == "fixed" else None
+        st_q = stored_count(name, "query", qry, pp, bits) if sectors == "fixed" else None
+        n_i = st_i["valid_kmers"] if st_i else kmer_count(ins, k, B)
+        n_q = st_q["valid_kmers"] if st_q else kmer_count(qry, k, B)
         line = {"suite": name, "alphabet": alphabet, "k": k, "m": m, "s": s, "H": H, "sectors": sectors,
                 "filter_bits": bits, "specialized": sbf.specialized,
-                "insert_kmers": kmer_count(ins, k, B), "query_kmers": kmer_count(qry, k, B),
-                "insert_kmers_per_s": kmer_count(ins, k, B) / t_ins,
-                "query_kmers_per_s": kmer_count(qry, k, B) / t_q, "fpr": fpr,
+                "insert_kmers": n_i, "query_kmers": n_q,
+                "kmers_counted": "valid k-mers (oracle count)" if st_i and st_q else "k-mer positions",
+                "insert_kmers_per_s": n_i / t_ins,
+                "query_kmers_per_s": n_q / t_q, "fpr": fpr,
                 "fpr_kmers": n_fpr}
         line.update(extra or {})
         print(json.dumps(line), flush=True)

@@ -74,3 +74,21 @@ def test_kernel_hash_sees_code_not_comments():
     assert bench.code_only(src.replace("b =", "c =")) != bench.code_only(src)
     stored = bench.MEASURED_TRAFFIC["out-of-cache"]["source_sha"]
     assert len(stored) == 16 and len(bench.kernel_source_sha()) == 16
+
+
+def test_stored_counts_match_only_their_own_input():
+    """The bench takes the oracle's stored counts (valid k-mers, runs) only for
+    the exact input they were computed on: the tiny workload matches, a copy
+    with one base changed or other parameters does not."""
+    ins, qry = synth.tiny()
+    bits = 1 << 20
+    rec = bench.stored_count("tiny", "insert", ins, bench.MAIN, bits)
+    assert rec is not None and rec["valid_kmers"] == bench.kmer_count(ins)
+    assert bench.stored_count("tiny", "query", qry, bench.MAIN, bits)["valid_kmers"] == bench.kmer_count(qry)
+    seq = ins.seq.copy()
+    seq[0] = ord("A") if seq[0] != ord("A") else ord("C")
+    assert bench.stored_count("tiny", "insert", synth.Workload(seq, ins.offsets), bench.MAIN, bits) is None
+    assert bench.stored_count("tiny", "insert", ins, dict(bench.MAIN, H=2), bits) is None
+    assert bench.stored_count("tiny", "insert", ins, bench.MAIN, bits << 1) is None
+    runs, src = bench.exact_runs("tiny", "insert", ins, bench.MAIN, bits)
+    assert src.startswith("exact") and runs == rec["runs"]
