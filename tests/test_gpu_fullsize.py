@@ -165,3 +165,62 @@ def test_alphabet_workload_full(torch, alphabet):
     starts = qry.offsets[:-1][qry.meta["is_random"]][:20000]
     pos = (starts[:, None] + B * np.arange(flen // B - params["k"] + 1)[None, :]).reshape(-1)
     assert answer_bits(words, pos).mean() < 0.01
+
+
+@pytest.mark.parametrize("alphabet,params", [
+    ("dna", MAIN), ("protein", dict(k=12, m=8, s=10, H=4)), ("dna_triplet", dict(k=10, m=5, s=8, H=4))])
+def test_filter_beyond_2_31_shards(torch, alphabet, params):
+    """The largest filters: 2^40 bits = 2^32 shards (128 GiB), past the strip
+    kernels' 2^31-shard run keys, so the runtime-parameter kernel (DNA) and
+    the tiled alphabet kernels take them, with shard word indices beyond 2^32.
+    A few Mbp are inserted; every answer bit of a query batch that reaches
+    the inserted shards (the records themselves and reads of them at 5 %
+    substitution, whose s-mers test bits the image may or may not hold) and
+    of uniform reads equals the oracle's answer on its sparse image of the
+    same insert."""
+    import oracle as orc
+    free, _ = torch.cuda.mem_get_info()
+    if free < (1 << 37) + (8 << 30):
+        pytest.skip("needs 136 GiB of free device memory")
+    k, m, s, H = params["k"], params["m"], params["s"], params["H"]
+    shards, seed = 1 << 32, 41
+    rng = np.random.default_rng(4100 + len(alphabet))
+    if alphabet == "protein":
+        ins = synth.random_protein_records(rng, 60, 5_000, 40_000, lower_prob=0.01, junk_prob=0.001)
+        symbols, read_len = synth.AMINO20, 50
+    else:
+        ins = synth.random_records(rng, 40, 20_000, 60_000, n_prob=0.001, lower_prob=0.01)
+        symbols, read_len = synth.ACGT, 150
+    reads, roff, _ = synth.sample_reads(rng, ins.seq, ins.offsets, 20_000, 5_000, read_len, 0.05, symbols)
+    qseq = np.concatenate([ins.seq, reads])
+    qoff = np.concatenate([ins.offsets, ins.offsets[-1] + roff[1:]])
+    sbf = _filter(1 << 40, params, seed, alphabet)
+    try:
+        assert sbf.num_shards == shards
+        dseq, doff = to_dev(torch, ins.seq, ins.offsets)
+        sbf.insert(dseq, doff)
+        dq, dqo = to_dev(torch, qseq, qoff)
+        words = _gpu_words(torch, sbf, dq, dqo, int(qoff[-1]))
+        assert sbf.status() == 0
+    finally:
+        sbf.close()
+    keys, rows = orc.insert_sparse(ins.seq, ins.offsets, k, m, s, H, shards, seed, alphabet)
+
+    def shard_words(req):
+        req = np.asarray(req, dtype=np.uint64)
+        out = np.zeros((req.size, 4), dtype=np.uint64)
+        if keys.size:
+            idx = np.minimum(np.searchsorted(keys, req), keys.size - 1)
+            found = keys[idx] == req
+            out[found] = rows[idx[found]]
+        return out
+
+    positions = np.arange(int(qoff[0]), int(qoff[-1]), dtype=np.int64)
+    want = orc.query_sampled(shard_words, qseq, qoff, positions, k, m, s, H, shards, seed, alphabet)
+    got = answer_bits(words, positions)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} answers differ, first at position {positions[bad[0]]}"
+    # the inserted records' own k-mers all answer present; some mutated ones do not
+    own = positions < int(ins.offsets[-1])
+    assert want[own].sum() > 0 and (want[~own] != got[~own]).sum() == 0
+    assert 0 < want[~own].mean() < 1
