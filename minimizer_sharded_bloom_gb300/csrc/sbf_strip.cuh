@@ -81,45 +81,44 @@ __device__ __forceinline__ void flush_run(uint64_t *F, const uint32_t acc[8]) {
     }
 }
 
-// Cooperative flush over the warp's active lanes `am`: the runs that end at
-// this step (`flush` set, the run's shard in `key`, its masks in `acc`) are
-// reduced as (run, word) pairs spread over the active lanes, pair 4r + w to
-// the lane of rank (4r + w) mod n_active, so a run's four words leave in one
-// instruction (when four or more lanes are active) and reach L2 as one
-// 32-byte sector request instead of four.  The loop's trip count,
-// ceil(4 * runs / n_active) <= 128, is the same on every lane.
+// Cooperative flush over the warp's active lanes `am` (protein and triplet
+// inserts, whose runs are short): the runs that end at this step are written
+// to the warp's staging area (st_key, st_acc: 32 runs) at their rank among
+// the flushing lanes, then the active lanes reduce them as (run, word) pairs,
+// pair 4r + w on the lane of rank (4r + w) mod n_active, so a run's four
+// words leave in one instruction and reach L2 as one 32-byte request.  The
+// trip count, ceil(4 * runs / n_active) <= 128, is the same on every active
+// lane.
 template <int H>
 __device__ __forceinline__ void flush_coop(uint64_t *words, uint32_t key, const uint32_t acc[8], bool flush,
-                                           unsigned am) {
+                                           unsigned am, uint32_t *st_key, uint4 *st_acc) {
     const unsigned fm = __ballot_sync(am, flush);
     if (!fm) return;
     const int lane = threadIdx.x & 31;
-    const int rank = __popc(am & ((1u << lane) - 1u));
+    const unsigned lt = (1u << lane) - 1u;
+    if (flush) {
+        const int e = __popc(fm & lt);
+        st_key[e] = key;
+        st_acc[2 * e] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+        st_acc[2 * e + 1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncwarp(am);
+    const int rank = __popc(am & lt);
     const int n_act = __popc(am);
     const int pairs = 4 * __popc(fm);
     for (int base = 0; base < pairs; base += n_act) {
         const int pidx = base + rank;
-        const int rr = pidx >> 2, wd = pidx & 3;
-        // source lane: the rr-th (from 0) set bit of fm, clearing at most 31 bits
-        unsigned m = fm;
-        for (int j = 0; j < rr && j < 31; ++j) m &= m - 1u;
-        const int src = (pidx < pairs && m) ? __ffs(m) - 1 : __ffs(fm) - 1;
-        const uint32_t k = __shfl_sync(am, key, src);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t l = __shfl_sync(am, acc[2 * q], src);
-            const uint32_t h = __shfl_sync(am, acc[2 * q + 1], src);
-            if (wd == q) {
-                lo = l;
-                hi = h;
+        if (pidx < pairs) {
+            const int rr = pidx >> 2, wd = pidx & 3;
+            const uint2 v = reinterpret_cast<const uint2 *>(st_acc + 2 * rr)[wd];
+            if (wd < H && (v.x | v.y)) {
+                const uint64_t x = ((uint64_t)v.y << 32) | v.x;
+                asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)st_key[rr] * 4 + wd), "l"(x)
+                             : "memory");
             }
         }
-        if (pidx < pairs && wd < H && (lo | hi)) {
-            const uint64_t v = ((uint64_t)hi << 32) | lo;
-            asm volatile("red.global.or.b64 [%0], %1;" ::"l"(words + (uint64_t)k * 4 + wd), "l"(v) : "memory");
-        }
     }
+    __syncwarp(am);
 }
 
 // A run head's shard in pass B: from its slot when `staged`, else straight
@@ -466,6 +465,10 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
     constexpr int QN = 128;
     __shared__ __align__(16) uint32_t fq_acc[kQueue ? (NT / 32) * QN * 8 : 1];
     __shared__ uint32_t fq_key[kQueue ? (NT / 32) * QN : 1];
+    // protein and triplet insert: the cooperative flush's per-warp staging
+    constexpr bool kCoopSmem = !kQuery && A != 0;
+    __shared__ __align__(16) uint4 cs_acc[kCoopSmem ? (NT / 32) * 64 : 1];
+    __shared__ uint32_t cs_key[kCoopSmem ? (NT / 32) * 32 : 1];
 
     if (*reinterpret_cast<volatile int *>(a.status) & kStatusBadOffsets) return;
     if (a.wait_test > 0) {
@@ -962,7 +965,8 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                             } else if constexpr (A == 0) {
                                 if (key != cur_key && !(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                             } else {
-                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am);
+                                flush_coop<H>(words, cur_key, acc, key != cur_key && !(cur_key >> 31), am,
+                                              cs_key + (tid >> 5) * 32, cs_acc + (tid >> 5) * 64);
                             }
                             const uint32_t same = key == cur_key ? 1u : 0u;
 #pragma unroll
@@ -1014,7 +1018,8 @@ __global__ void __launch_bounds__(StripCfg<K, M, S, H, A, D>::NT) strip_kernel(L
                 } else if constexpr (A == 0) {
                     if (!(cur_key >> 31)) flush_run<H>(words + (uint64_t)cur_key * 4, acc);
                 } else {
-                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am);
+                    flush_coop<H>(words, cur_key, acc, !(cur_key >> 31), am, cs_key + (tid >> 5) * 32,
+                                  cs_acc + (tid >> 5) * 64);
                 }
             }
         }
