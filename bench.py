@@ -376,6 +376,29 @@ def cpu_baseline(ins, qry, bits: int, budget_bases: int = 40_000_000, reads: int
     return res
 
 
+def workload_config(workload: str, spec, p, ins, qry) -> dict:
+    """The keys of a line's `config` that identify its workload, the same in
+    both arms: parameters, filter size, and the batches' bases, k-mer
+    positions, valid k-mers (the oracle's stored count where it matches) and
+    records, plus which of the counts the k-mers/s divide by."""
+    B = sym_bytes(p)
+    pos_ins, pos_q = kmer_count(ins, p["k"], B), kmer_count(qry, p["k"], B)
+    st_ins = stored_count(workload, "insert", ins, p, spec["bits"])
+    st_q = stored_count(workload, "query", qry, p, spec["bits"])
+    return {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
+            "alphabet": p["alphabet"], "seed": SEED, "filter_bits": spec["bits"],
+            "insert_kmers": st_ins["valid_kmers"] if st_ins else pos_ins,
+            "query_kmers": st_q["valid_kmers"] if st_q else pos_q,
+            "kmers_counted": ("valid k-mers (the oracle's count of this input)" if st_ins and st_q
+                              else "k-mer positions (no stored oracle count of this input)"),
+            "insert_bases": int(ins.offsets[-1] - ins.offsets[0]),
+            "query_bases": int(qry.offsets[-1] - qry.offsets[0]),
+            "insert_kmer_positions": pos_ins, "query_kmer_positions": pos_q,
+            "insert_valid_kmers": st_ins["valid_kmers"] if st_ins else None,
+            "query_valid_kmers": st_q["valid_kmers"] if st_q else None,
+            "insert_records": int(ins.n_records), "query_records": int(qry.n_records)}
+
+
 def run_reference(args, workload):
     """The reference arm: the CPU oracle on the host cores, one bounded sample
     of the workload per step."""
@@ -396,9 +419,9 @@ def run_reference(args, workload):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
-                       "alphabet": p["alphabet"],
-                       "filter_bits": spec["bits"], "timing": "host wall clock per sample"},
+            "config": dict(workload_config(workload, spec, p, ins, qry),
+                           timing="host wall clock per sample (the oracle on a bounded sample of "
+                                  "the workload; cpu_baseline.sample says which)"),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "k-mers/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -456,13 +479,8 @@ def main():
     ins, qry = spec["make"]()
     # k-mers/s counts valid k-mers: the oracle's count of this input where a
     # stored one matches (the k-mer positions of clean records are all valid)
-    pos_ins, pos_q = kmer_count(ins, p["k"], B), kmer_count(qry, p["k"], B)
-    st_ins = stored_count(args.workload, "insert", ins, p, spec["bits"])
-    st_q = stored_count(args.workload, "query", qry, p, spec["bits"])
-    nk_ins = st_ins["valid_kmers"] if st_ins else pos_ins
-    nk_q = st_q["valid_kmers"] if st_q else pos_q
-    kmers_counted = ("valid k-mers (the oracle's count of this input)" if st_ins and st_q
-                     else "k-mer positions (no stored oracle count of this input)")
+    wcfg = workload_config(args.workload, spec, p, ins, qry)
+    nk_ins, nk_q = wcfg["insert_kmers"], wcfg["query_kmers"]
 
     dseq = torch.from_numpy(ins.seq).cuda()
     doff = torch.from_numpy(ins.offsets).cuda()
@@ -632,16 +650,7 @@ def main():
             "ms_per_step": 1e3 * step_s, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8/u64 (integer)",
             "data": "synthetic",
-            "config": {"workload": spec["desc"], "k": p["k"], "m": p["m"], "s": p["s"], "H": p["H"],
-                       "alphabet": p["alphabet"], "seed": SEED,
-                       "filter_bits": spec["bits"], "insert_kmers": nk_ins, "query_kmers": nk_q,
-                       "kmers_counted": kmers_counted,
-                       "insert_bases": int(ins.offsets[-1] - ins.offsets[0]),
-                       "query_bases": int(qry.offsets[-1] - qry.offsets[0]),
-                       "insert_kmer_positions": pos_ins, "query_kmer_positions": pos_q,
-                       "insert_valid_kmers": st_ins["valid_kmers"] if st_ins else None,
-                       "query_valid_kmers": st_q["valid_kmers"] if st_q else None,
-                       "insert_records": n_ins, "query_records": n_q,
+            "config": dict(wcfg, **{
                        "l2": {"out-of-cache": "inputs larger than L2 (sequences 1 GB each, filter 8 GiB)",
                               "protein-like": "inputs larger than L2 (sequences 0.5 GB each, filter 1 GiB)",
                               "triplet": "inputs larger than L2 (sequences 1 GB each, filter 1 GiB)"}
@@ -650,7 +659,7 @@ def main():
                                                "the events; it also flushes L2)",
                        "timing": "CUDA events around each call on the launching stream; value and "
                                  "ms_per_step from the median insert + median query",
-                       "replicas": world},
+                       "replicas": world}),
             "insert_kmers_per_s": throughput(world, 1, nk_ins, med_ins),
             "query_kmers_per_s": throughput(world, 1, nk_q, med_q),
             "insert_ms": {"median": 1e3 * med_ins, "mean": 1e3 * mean_ins, "all": [1e3 * t for t in t_ins]},

@@ -63,6 +63,11 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "k-mers/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # the workload is identified by the same keys as the GPU arm's line
+    ins, qry = synth.tiny()
+    want = bench.workload_config("tiny", bench.WORKLOADS["tiny"], bench.MAIN, ins, qry)
+    assert {k: d["config"][k] for k in want} == want
+    assert want["kmers_counted"].startswith("valid k-mers") and want["insert_kmers"] == 99_970
 
 
 def test_kernel_hash_sees_code_not_comments():
