@@ -140,9 +140,9 @@ def test_uniform_reads_give_whole_dense_ready_chunks(driver):
 
 def test_chunk_sizes_grow_and_a_query_tail_shrinks(driver):
     """Full-size policy on 2,000,000 reads of 150 bp (3 * 10^8 positions,
-    default 2^26 chunk): chunks start near 2^22 positions and double up to an
-    eighth of the batch (37.5 M positions, under 2^26); a query's last chunks
-    shrink again, an insert's do not; every chunk stays whole."""
+    a 2^26 chunk setting): chunks start near 2^22 positions and double up to
+    an eighth of the batch (37.5 M positions, under 2^26); a query's last
+    chunks shrink again, an insert's do not; every chunk stays whole."""
     off = synth.csr(np.full(2_000_000, 150))
     for query in (False, True):
         chunk_max, chunks = plan(driver, off, 1 << 26, 31, 1, query)
@@ -157,6 +157,21 @@ def test_chunk_sizes_grow_and_a_query_tail_shrinks(driver):
             assert tail[-1] < 1 << 24 and tail == sorted(tail, reverse=True)
         else:
             assert sizes[-2] > chunk_max - 64 * 150
+
+
+def test_library_default_chunk_on_the_benchmark_read_batch(driver):
+    """The library's default chunk setting (2^25 positions) on the benchmark's
+    6,666,666 reads of 150 bp: chunks are capped at 2^25 positions (under an
+    eighth of the batch), stay whole and end at read starts, so every chunk
+    runs as a uniform batch; the query's tail shrinks below 2^23."""
+    off = synth.csr(np.full(6_666_666, 150))
+    chunk_max, chunks = plan(driver, off, 1 << 25, 31, 1, True)
+    assert chunk_max == 1 << 25
+    check_plan(off, chunk_max, chunks, 1 << 25, 31, 1, True, per_position=False)
+    sizes = [c["ce"] - c["cs"] for c in chunks]
+    assert max(sizes) <= 1 << 25 and all(c["whole"] for c in chunks)
+    assert all(c["cs"] % 150 == 0 for c in chunks)
+    assert sizes[-1] < 1 << 23
 
 
 def test_small_batch_is_one_chunk(driver):
