@@ -100,7 +100,6 @@ class SuperBloomFilter:
                     out.data_ptr(), _stream_handle(stream))
         return out
 
-    # ---- host-resident (synchronising) ------------------------------------
     def query_dense(self, seq: torch.Tensor, record_len: int, out: torch.Tensor | None = None,
                     stream=None) -> torch.Tensor:
         """Query a dense batch of fixed-length records (seq.numel() //
@@ -112,6 +111,7 @@ class SuperBloomFilter:
         N.sbf_query_dense(self._h, seq.data_ptr(), n, record_len, out.data_ptr(), _stream_handle(stream))
         return out
 
+    # ---- host-resident (synchronising) ------------------------------------
     def insert_host(self, seq: np.ndarray, offsets: np.ndarray) -> None:
         seq = np.ascontiguousarray(seq, dtype=np.uint8)
         offsets = np.ascontiguousarray(offsets, dtype=np.int64)
